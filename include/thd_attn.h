@@ -1,0 +1,174 @@
+/*
+ * thd_attn.h -- C ABI of the GB300 (sm_103a) packed-THD forward attention library.
+ *
+ * Operation (scaled-dot-product attention forward with log-sum-exp Stats over a
+ * packed, ragged "THD" batch):
+ *
+ *   for each sequence b and query head h (kv head g = h / (h_q / h_kv)):
+ *     len_q = cu_seqlens_q[b+1] - cu_seqlens_q[b],  len_k = cu_seqlens_kv[b+1] - cu_seqlens_kv[b]
+ *     q_i = Q[off_q[b] + i, h, :],  k_j = K[off_k[b] + j, g, :],  v_j = V[off_v[b] + j, g, :]
+ *     s_ij = softmax_scale * <q_i, k_j>
+ *     visible(i, j) = j < len_k  and  (mask 0: true | mask 1: j <= i | mask 2: j <= i + c)
+ *         c = q_causal_offset[b], or len_k - len_q when q_causal_offset is NULL
+ *     LSE_i = ln sum_{visible j} exp(s_ij)               (natural log, scaled scores)
+ *     O_i   = sum_{visible j} exp(s_ij - LSE_i) * v_j
+ *     rows with no visible key: O_i = 0, LSE_i = -inf
+ *     O[off_o[b] + i, h, :] = O_i ;  Stats[(off_s[b] + i) * st_tok + h * st_head] = LSE_i
+ *
+ *   Every other row of O and Stats is left untouched (pad rows are never written).
+ *
+ * Where each piece comes from:
+ *   - per-tensor ragged offsets, read on the device instead of re-deriving
+ *     prefix(lens) x stride; lengths still drive the mask bounds and dead rows:
+ *     cuDNN-frontend issue "THD lowering never reads the bound ragged offsets",
+ *     sections "Concrete failure" and "Proposal: consume the bound offsets on device";
+ *   - cu_seqlens / cu_seqlens_padded vocabulary, per-sequence mask policy as an
+ *     on-device tensor, no host synchronisation in the call:
+ *     TransformerEngine PR #3274, review comments on pad_between_seqs and
+ *     attn_mask_type_per_seq;
+ *   - q_causal_offset ("global token index of each segment's local q[0]") and
+ *     bottom-right alignment for context-parallel chunks: Megatron-LM PR #14
+ *     "fix(dsa): align packed-CP indexer causal masks";
+ *   - Stats layouts token-major [t,h] and head-major [h,t], the all-axes span rule
+ *     for capacities, and the persistent scheduler's tile counter at word 0 of the
+ *     workspace: NVIDIA/cudnn-frontend PR #462, sections "What", "Root cause" and
+ *     "The fix".
+ *   - 16-byte alignment of pointers and token strides: cudnn-frontend PR #516
+ *     (ragged token-stride gaps), squashed commit text.
+ *
+ * Conventions:
+ *   - All tensors are caller-owned device memory. The library allocates no device
+ *     memory in thd_attn_fwd; scratch lives in the caller's workspace.
+ *   - Offsets are ROW units per tensor; element address of (row, head, e) in Q/K/V/O
+ *     is base + row * stride_tok + head * stride_head + e (elements; last dim contiguous).
+ *   - Host-side errors are returned as thd_status_t; nothing aborts or throws.
+ *   - Device-side data errors (bad lengths/offsets/mask values) are recorded as bits
+ *     in a status word inside the workspace; the affected sequence gets no work and
+ *     its rows stay untouched. thd_attn_read_status copies that word to the host.
+ *   - thd_attn_fwd is asynchronous on the given stream, performs no device->host
+ *     read and no allocation, and may be captured in a CUDA graph.
+ */
+#ifndef THD_ATTN_H
+#define THD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  THD_OK = 0,
+  THD_ERR_INVALID_ARG = 1,   /* bad descriptor field or NULL pointer */
+  THD_ERR_UNSUPPORTED = 2,   /* valid request the selected kernel cannot serve */
+  THD_ERR_ALIGNMENT = 3,     /* pointer or stride not 16-byte aligned where required */
+  THD_ERR_CAPACITY = 4,      /* a tensor view's all-axes span exceeds its declared bytes */
+  THD_ERR_WORKSPACE = 5,     /* workspace NULL, too small, or misaligned */
+  THD_ERR_CUDA = 6           /* a CUDA runtime call or kernel launch failed */
+} thd_status_t;
+
+typedef enum { THD_BF16 = 0, THD_FP16 = 1, THD_FP32 = 2 } thd_dtype_t;
+
+/* Stats (LSE) layout: token-major [t, h] (token stride h_q, head stride 1) or
+ * head-major [h, t] (token stride 1, head stride cap_rows_stats). */
+typedef enum { THD_STATS_TOKEN_MAJOR = 0, THD_STATS_HEAD_MAJOR = 1 } thd_stats_layout_t;
+
+/* Kernel choice. AUTO takes the tcgen05 tensor-core kernel where it applies
+ * (bf16/fp16, d in {64, 128}, 16-byte aligned rows) and the SIMT kernel
+ * otherwise; the other two force one (TCGEN05 fails with THD_ERR_UNSUPPORTED
+ * when it does not apply). */
+typedef enum { THD_KERNEL_AUTO = 0, THD_KERNEL_SIMT = 1, THD_KERNEL_TCGEN05 = 2 } thd_kernel_t;
+
+/* Mask policy values of the per-sequence mask_type tensor. */
+enum { THD_MASK_NONE = 0, THD_MASK_CAUSAL_TOP_LEFT = 1, THD_MASK_CAUSAL_BOTTOM_RIGHT = 2 };
+
+/* Bits of the device status word (thd_attn_read_status). */
+enum {
+  THD_DEV_BAD_LENGTH = 1u << 0,     /* cu_seqlens not non-decreasing for some b */
+  THD_DEV_BAD_OFFSET = 1u << 1,     /* off[b] < 0 or off[b] + len > cap_rows for some tensor */
+  THD_DEV_BAD_MASK = 1u << 2,       /* mask_type[b] not in {0, 1, 2} */
+  THD_DEV_TILE_OVERFLOW = 1u << 3,  /* more query tiles than the plan's capacity (no work done) */
+  THD_DEV_WAIT_TIMEOUT = 1u << 4    /* a bounded in-kernel wait gave up (kernel returned early) */
+};
+
+/* Host-known problem description, fixed per plan. Index 0..3 of the stride and
+ * capacity arrays is Q, K, V, O. */
+typedef struct {
+  thd_dtype_t dtype;              /* storage type of Q, K, V and O */
+  int32_t batch;                  /* B, number of sequences (>= 0) */
+  int32_t h_q, h_kv, d;           /* heads and head dim; h_q % h_kv == 0; 1 <= d <= 128 */
+  int64_t cap_rows[4];            /* physical rows of the Q, K, V, O views */
+  int64_t stride_tok[4];          /* elements between consecutive rows */
+  int64_t stride_head[4];         /* elements between consecutive heads */
+  int64_t bytes[4];               /* allocation size behind each pointer (bytes); the view's
+                                     all-axes span must fit. 0 = not checked */
+  int64_t cap_rows_stats;         /* physical rows of Stats (T_s) */
+  thd_stats_layout_t stats_layout;
+  float softmax_scale;            /* NaN => 1/sqrt(d) */
+  thd_kernel_t kernel;
+} thd_attn_desc_t;
+
+typedef struct thd_attn_plan_s* thd_attn_plan_t;
+
+/* Validate the descriptor and pick the kernel (host only: no CUDA call, no device
+ * read). On success *out owns a plan (free with thd_attn_plan_destroy) and
+ * *workspace_bytes is the scratch the fwd call needs (256-byte aligned device
+ * memory; its first word is the persistent scheduler's tile counter). */
+thd_status_t thd_attn_plan(thd_attn_plan_t* out, const thd_attn_desc_t* desc,
+                           size_t* workspace_bytes);
+
+/* Enqueue the forward pass on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   q, k, v, o        device pointers to the views described by the plan
+ *   stats             device float32 LSE buffer (layout per plan)
+ *   cu_seqlens_q/kv   device int32 [B+1]; per-sequence lengths are the differences
+ *   off_q .. off_s    device int32 [>= B] row offset of each sequence's first row in
+ *                     Q, K, V, O and Stats (a cu_seqlens_padded array may be passed
+ *                     directly; entry B is not read)
+ *   mask_type         device int8 [B], values THD_MASK_*
+ *   q_causal_offset   device int32 [B] or NULL (NULL => len_k - len_q for mask 2;
+ *                     ignored for masks 0 and 1)
+ *   workspace         device memory of >= workspace_bytes, 256-byte aligned
+ * Returns THD_OK once both kernels are enqueued. Device data errors surface only
+ * through thd_attn_read_status. Sequences whose O (or Stats) rows overlap race. */
+thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, const void* v,
+                          void* o, float* stats, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_kv, const int32_t* off_q,
+                          const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
+                          const int32_t* off_s, const int8_t* mask_type,
+                          const int32_t* q_causal_offset, void* workspace, void* stream);
+
+/* Copy the device status word of the last fwd on this workspace to *host_out and
+ * synchronise `stream`. This is the only call that waits on the device. */
+thd_status_t thd_attn_read_status(thd_attn_plan_t plan, const void* workspace,
+                                  uint32_t* host_out, void* stream);
+
+/* Which kernel the plan selected: THD_KERNEL_SIMT or THD_KERNEL_TCGEN05. */
+thd_kernel_t thd_attn_plan_kernel(thd_attn_plan_t plan);
+
+/* Tile geometry the plan uses (query rows per scheduled unit, keys per KV tile)
+ * and its capacity in scheduled (sequence, query-tile) pairs. */
+void thd_attn_plan_geometry(thd_attn_plan_t plan, int32_t* rows_per_unit,
+                            int32_t* keys_per_tile, int32_t* max_pairs);
+
+/* Byte offsets, inside the workspace, of its four regions: [0] header words
+ * (tile counter, status, pair count, tile count), [1] per-sequence metadata
+ * (8 int32 per sequence: len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift),
+ * [2] per-sequence first pair index (int32 [B+1]), [3] the scheduled pair list
+ * (int32 {b, first query row} per pair, longest first). For inspection only. */
+void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]);
+
+void thd_attn_plan_destroy(thd_attn_plan_t plan);
+
+const char* thd_attn_status_string(thd_status_t status);
+
+/* All-axes span in bytes of a strided view: ((rows-1)*s_t + (heads-1)*s_h + (d-1) + 1) * elem,
+ * 0 for an empty view (the workspace-sizing rule of cudnn-frontend PR #462, "The fix"). */
+int64_t thd_attn_view_span_bytes(int64_t rows, int64_t heads, int64_t d, int64_t stride_tok,
+                                 int64_t stride_head, int64_t elem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* THD_ATTN_H */

@@ -1,0 +1,15 @@
+"""CPU oracle for packed-THD forward attention -- test infrastructure only.
+
+Imported by ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py``; never by the library. Shares no code with the CUDA path.
+"""
+from .thd_attention import (MASK_CAUSAL_BOTTOM_RIGHT, MASK_CAUSAL_TOP_LEFT, MASK_NONE,
+                            attention_one_head, causal_shift, thd_attention_fwd,
+                            unmasked_entries, visible_key_count)
+from .brute import brute_attention
+
+__all__ = [
+    "MASK_NONE", "MASK_CAUSAL_TOP_LEFT", "MASK_CAUSAL_BOTTOM_RIGHT", "attention_one_head",
+    "causal_shift", "thd_attention_fwd", "unmasked_entries", "visible_key_count",
+    "brute_attention",
+]

@@ -1,0 +1,236 @@
+"""ctypes binding of ``libthd_attn.so`` (declared in ``include/thd_attn.h``).
+
+Argument marshalling only: torch tensors become device pointers, strides and
+sizes; every step of the forward pass runs in the library's CUDA kernels. There
+is no fallback -- when the library is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+STATS_TOKEN_MAJOR, STATS_HEAD_MAJOR = 0, 1
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05 = 0, 1, 2
+_DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+_STATUS = {0: "THD_OK", 1: "THD_ERR_INVALID_ARG", 2: "THD_ERR_UNSUPPORTED",
+           3: "THD_ERR_ALIGNMENT", 4: "THD_ERR_CAPACITY", 5: "THD_ERR_WORKSPACE",
+           6: "THD_ERR_CUDA"}
+
+# device status word bits
+DEV_BAD_LENGTH, DEV_BAD_OFFSET, DEV_BAD_MASK, DEV_TILE_OVERFLOW, DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+
+
+class ThdAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)}")
+        self.status = status
+
+
+class ThdAttnDesc(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("batch", ctypes.c_int32),
+        ("h_q", ctypes.c_int32),
+        ("h_kv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("cap_rows", ctypes.c_int64 * 4),
+        ("stride_tok", ctypes.c_int64 * 4),
+        ("stride_head", ctypes.c_int64 * 4),
+        ("bytes", ctypes.c_int64 * 4),
+        ("cap_rows_stats", ctypes.c_int64),
+        ("stats_layout", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float),
+        ("kernel", ctypes.c_int),
+    ]
+
+
+_LIB = None
+_EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_plan_kernel",
+            "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
+            "thd_attn_status_string", "thd_attn_view_span_bytes"]
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libthd_attn.so")
+
+
+def load_library():
+    """Load the C-ABI library once; raise if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with ragged_varlen_attention_gb300.build")
+    lib = ctypes.CDLL(path)
+    vp, i32p, i64p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    lib.thd_attn_plan.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(ThdAttnDesc),
+                                  ctypes.POINTER(ctypes.c_size_t)]
+    lib.thd_attn_plan.restype = ctypes.c_int
+    lib.thd_attn_fwd.argtypes = [vp] * 17
+    lib.thd_attn_fwd.restype = ctypes.c_int
+    lib.thd_attn_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.thd_attn_read_status.restype = ctypes.c_int
+    lib.thd_attn_plan_kernel.argtypes = [vp]
+    lib.thd_attn_plan_kernel.restype = ctypes.c_int
+    lib.thd_attn_plan_geometry.argtypes = [vp, i32p, i32p, i32p]
+    lib.thd_attn_plan_geometry.restype = None
+    lib.thd_attn_plan_workspace_layout.argtypes = [vp, i64p]
+    lib.thd_attn_plan_workspace_layout.restype = None
+    lib.thd_attn_plan_destroy.argtypes = [vp]
+    lib.thd_attn_plan_destroy.restype = None
+    lib.thd_attn_status_string.argtypes = [ctypes.c_int]
+    lib.thd_attn_status_string.restype = ctypes.c_char_p
+    lib.thd_attn_view_span_bytes.argtypes = [ctypes.c_int64] * 6
+    lib.thd_attn_view_span_bytes.restype = ctypes.c_int64
+    _LIB = lib
+    return lib
+
+
+class ThdAttnPlan:
+    """Owns a ``thd_attn_plan_t``; frees it when collected."""
+
+    def __init__(self, handle: int, workspace_bytes: int, desc: ThdAttnDesc):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+        self.desc = desc
+        lib = load_library()
+        self.kernel = lib.thd_attn_plan_kernel(handle)
+        a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        lib.thd_attn_plan_geometry(handle, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+        self.rows_per_unit, self.keys_per_tile, self.max_pairs = a.value, b.value, c.value
+        offs = (ctypes.c_int64 * 4)()
+        lib.thd_attn_plan_workspace_layout(handle, offs)
+        self.workspace_layout = tuple(int(x) for x in offs)
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _LIB is not None:
+            _LIB.thd_attn_plan_destroy(self.handle)
+            self.handle = None
+
+
+def _view_bytes(t: torch.Tensor) -> int:
+    return t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+
+
+def make_desc(dtype: torch.dtype, batch: int, h_q: int, h_kv: int, d: int, cap_rows, stride_tok,
+              stride_head, nbytes=(0, 0, 0, 0), cap_rows_stats: int = 0,
+              stats_layout: int = STATS_TOKEN_MAJOR, softmax_scale: float | None = None,
+              kernel: int = KERNEL_AUTO) -> ThdAttnDesc:
+    desc = ThdAttnDesc()
+    desc.dtype = _DTYPE_CODE[dtype]
+    desc.batch, desc.h_q, desc.h_kv, desc.d = batch, h_q, h_kv, d
+    for i in range(4):
+        desc.cap_rows[i] = int(cap_rows[i])
+        desc.stride_tok[i] = int(stride_tok[i])
+        desc.stride_head[i] = int(stride_head[i])
+        desc.bytes[i] = int(nbytes[i])
+    desc.cap_rows_stats = int(cap_rows_stats)
+    desc.stats_layout = int(stats_layout)
+    desc.softmax_scale = math.nan if softmax_scale is None else float(softmax_scale)
+    desc.kernel = int(kernel)
+    return desc
+
+
+def thd_attn_plan(desc: ThdAttnDesc) -> ThdAttnPlan:
+    lib = load_library()
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.thd_attn_plan(ctypes.byref(handle), ctypes.byref(desc), ctypes.byref(ws))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_plan")
+    return ThdAttnPlan(handle.value, ws.value, desc)
+
+
+def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: int,
+                     softmax_scale=None, kernel: int = KERNEL_AUTO) -> ThdAttnPlan:
+    """Build a plan from [rows, heads, d] tensor views (last dim contiguous)."""
+    for t in (q, k, v, o):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("Q/K/V/O must be [rows, heads, d] views with a contiguous last dim")
+    desc = make_desc(q.dtype, batch, q.shape[1], k.shape[1], q.shape[2],
+                     [t.shape[0] for t in (q, k, v, o)], [t.stride(0) for t in (q, k, v, o)],
+                     [t.stride(1) for t in (q, k, v, o)], [_view_bytes(t) for t in (q, k, v, o)],
+                     cap_rows_stats, stats_layout, softmax_scale, kernel)
+    return thd_attn_plan(desc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def thd_attn_fwd(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k,
+                 off_v, off_o, off_s, mask_type, q_causal_offset, workspace, stream=None) -> None:
+    """Enqueue the forward pass (see ``thd_attn_fwd`` in include/thd_attn.h)."""
+    lib = load_library()
+    st = lib.thd_attn_fwd(ctypes.c_void_p(plan.handle), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                          _ptr(stats), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(off_q),
+                          _ptr(off_k), _ptr(off_v), _ptr(off_o), _ptr(off_s), _ptr(mask_type),
+                          _ptr(q_causal_offset), _ptr(workspace), _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_fwd")
+
+
+def thd_attn_read_status(plan: ThdAttnPlan, workspace, stream=None) -> int:
+    lib = load_library()
+    out = ctypes.c_uint32()
+    st = lib.thd_attn_read_status(ctypes.c_void_p(plan.handle), _ptr(workspace), ctypes.byref(out),
+                                  _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_read_status")
+    return out.value
+
+
+def alloc_workspace(plan: ThdAttnPlan, device) -> torch.Tensor:
+    n = max(256, (plan.workspace_bytes + 255) // 256 * 256)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+_PLAN_CACHE: dict = {}
+
+
+def thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=None, off_v=None,
+                     off_o=None, off_s=None, mask_type=None, q_causal_offset=None, o=None,
+                     stats=None, stats_layout: int = STATS_TOKEN_MAJOR, softmax_scale=None,
+                     kernel: int = KERNEL_AUTO, workspace=None, stream=None):
+    """One-call forward over device tensors.
+
+    Offsets default to the cu_seqlens arrays (packed layout); ``mask_type``
+    defaults to no mask. O and Stats are allocated when not given (O with the
+    shape of Q; Stats with Q's rows). Returns ``(o, stats)``.
+    """
+    batch = cu_seqlens_q.numel() - 1
+    dev = q.device
+    off_q = cu_seqlens_q if off_q is None else off_q
+    off_k = cu_seqlens_kv if off_k is None else off_k
+    off_v = off_k if off_v is None else off_v
+    off_o = off_q if off_o is None else off_o
+    off_s = off_o if off_s is None else off_s
+    if mask_type is None:
+        mask_type = torch.zeros(max(batch, 1), dtype=torch.int8, device=dev)
+    if o is None:
+        o = torch.zeros(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=dev)
+    if stats is None:
+        stats = torch.full((q.shape[0] * q.shape[1],), float("-inf"), dtype=torch.float32, device=dev)
+    cap_s = stats.numel() // q.shape[1]
+    key = (q.dtype, batch, tuple(q.shape), tuple(k.shape), tuple(v.shape), tuple(o.shape),
+           q.stride(), k.stride(), v.stride(), o.stride(), cap_s, stats_layout, softmax_scale, kernel,
+           _view_bytes(q), _view_bytes(k), _view_bytes(v), _view_bytes(o))
+    plan = _PLAN_CACHE.get(key)
+    if plan is None:
+        plan = plan_for_tensors(q, k, v, o, batch, cap_s, stats_layout, softmax_scale, kernel)
+        _PLAN_CACHE[key] = plan
+    if workspace is None:
+        workspace = alloc_workspace(plan, dev)
+    thd_attn_fwd(plan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v, off_o,
+                 off_s, mask_type, q_causal_offset, workspace, stream)
+    return o, stats

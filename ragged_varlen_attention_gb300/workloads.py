@@ -1,0 +1,269 @@
+"""Seeded synthetic packed-THD batches.
+
+This module only draws inputs: sequence lengths, gap sizes, mask choices and
+N(0, 1) tensor values, and lays them out in rows. It holds none of the
+attention arithmetic, so both the CUDA path's tests/bench and the CPU oracle
+can consume the same batch.
+
+Named workloads (shapes follow the pages' packed-THD examples):
+
+* ``tiny_padded``      -- 3 sequences, lengths [3, 2, 4] with one identifier row after
+  each (cu_seqlens [0,3,5,9], cu_seqlens_padded [0,4,8,13]), h=2, d=16, fp32,
+  masks [causal, none, causal], token-major LSE.
+* ``padded_causal``    -- 8 sequences, lengths U{64..1024}, 0-16 pad rows after
+  each, h=16, d=128, bf16, top-left causal, head-major LSE.
+* ``mixed_gqa``        -- 32 sequences, lognormal lengths (median 512, clipped to
+  [16, 4096], ~32k tokens), 0-8 pad rows, h_q=32/h_kv=8, d=128, bf16, causal flag
+  ~ Bernoulli(0.5), token-major LSE.
+* ``cp_chunks``        -- 2 documents of 65536 keys, a 4096-row query chunk each at
+  causal offset k_len - q_len (bottom-right causal), h=16, d=128, bf16, head-major
+  LSE.
+* ``separate_padding`` -- 64 sequences, lengths U{0..4096} (one forced to 0), Q/O
+  rows padded to multiples of 64 with NaN, K/V packed with 1-row identifier gaps,
+  h=32, d=64, fp16, masks drawn from {none, causal, bottom-right causal},
+  token-major LSE.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+MASK_NONE, MASK_TOP_LEFT, MASK_BOTTOM_RIGHT = 0, 1, 2
+STATS_TOKEN_MAJOR, STATS_HEAD_MAJOR = 0, 1
+
+# byte pattern pre-filled into every output buffer; rows the kernel must not
+# touch are compared against it bit for bit
+SENTINEL_BYTE = 0xA5
+
+_TORCH_DTYPE = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+WORKLOAD_SEEDS = {"tiny_padded": 101, "padded_causal": 102, "mixed_gqa": 103,
+                  "cp_chunks": 104, "separate_padding": 105}
+
+
+@dataclass
+class ThdBatch:
+    """One packed-THD problem: metadata (host numpy) and tensors (host torch)."""
+    name: str
+    dtype: str
+    h_q: int
+    h_kv: int
+    d: int
+    cu_seqlens_q: np.ndarray      # int32 [B+1]
+    cu_seqlens_kv: np.ndarray     # int32 [B+1]
+    off_q: np.ndarray             # int32 [B+1] row offsets (entry B = end marker)
+    off_k: np.ndarray
+    off_v: np.ndarray
+    off_o: np.ndarray
+    off_s: np.ndarray
+    mask_type: np.ndarray         # int8 [B]
+    q_causal_offset: np.ndarray | None  # int32 [B] or None
+    stats_layout: int
+    q: torch.Tensor               # [cap_q, h_q, d] storage dtype
+    k: torch.Tensor               # [cap_k, h_kv, d]
+    v: torch.Tensor               # [cap_v, h_kv, d]
+    cap_o: int
+    cap_s: int
+    softmax_scale: float | None = None
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_seqlens_q) - 1
+
+    @property
+    def torch_dtype(self):
+        return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def stats_strides(self):
+        """(token stride, head stride) of the flat Stats buffer, in elements."""
+        if self.stats_layout == STATS_TOKEN_MAJOR:
+            return self.h_q, 1
+        return 1, self.cap_s
+
+    @property
+    def stats_numel(self) -> int:
+        return self.cap_s * self.h_q
+
+    def lens_q(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_q.astype(np.int64))
+
+    def lens_k(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_kv.astype(np.int64))
+
+    def o_init(self) -> torch.Tensor:
+        """Output buffer pre-filled with the sentinel byte pattern."""
+        t = torch.empty((self.cap_o, self.h_q, self.d), dtype=self.torch_dtype)
+        t.view(torch.uint8).fill_(SENTINEL_BYTE)
+        return t
+
+    def stats_init(self) -> torch.Tensor:
+        t = torch.empty((self.stats_numel,), dtype=torch.float32)
+        t.view(torch.uint8).fill_(SENTINEL_BYTE)
+        return t
+
+
+def _normal(rng: np.random.Generator, shape, dtype: str) -> torch.Tensor:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    return torch.from_numpy(x).to(_TORCH_DTYPE[dtype])
+
+
+def _fill_rows(t: torch.Tensor, rows: np.ndarray, value: float) -> None:
+    if len(rows):
+        t[torch.from_numpy(rows.astype(np.int64))] = value
+
+
+def _pad_rows(cap: int, starts: np.ndarray, lens: np.ndarray) -> np.ndarray:
+    """Rows of [0, cap) not covered by any [start, start+len)."""
+    used = np.zeros(cap, dtype=bool)
+    for s, n in zip(starts, lens):
+        used[s:s + n] = True
+    return np.nonzero(~used)[0]
+
+
+def _cumsum0(x) -> np.ndarray:
+    return np.concatenate([[0], np.cumsum(np.asarray(x, dtype=np.int64))]).astype(np.int32)
+
+
+def tiny_padded(seed: int = WORKLOAD_SEEDS["tiny_padded"]) -> ThdBatch:
+    rng = np.random.default_rng(seed)
+    cu = np.array([0, 3, 5, 9], dtype=np.int32)
+    padded = np.array([0, 4, 8, 13], dtype=np.int32)
+    cap, h, d = 13, 2, 16
+    q, k, v = (_normal(rng, (cap, h, d), "fp32") for _ in range(3))  # identifier rows: N(0,1)
+    return ThdBatch("tiny_padded", "fp32", h, h, d, cu, cu.copy(), padded, padded.copy(),
+                    padded.copy(), padded.copy(), padded.copy(),
+                    np.array([MASK_TOP_LEFT, MASK_NONE, MASK_TOP_LEFT], dtype=np.int8), None,
+                    STATS_TOKEN_MAJOR, q, k, v, cap, cap)
+
+
+def padded_causal(seed: int = WORKLOAD_SEEDS["padded_causal"]) -> ThdBatch:
+    rng = np.random.default_rng(seed)
+    b, h, d = 8, 16, 128
+    lens = rng.integers(64, 1024, size=b, endpoint=True)
+    gaps = rng.integers(0, 16, size=b, endpoint=True)
+    cu = _cumsum0(lens)
+    padded = _cumsum0(lens + gaps)
+    cap = int(padded[-1])
+    q, k, v = (_normal(rng, (cap, h, d), "bf16") for _ in range(3))
+    pads = _pad_rows(cap, padded[:-1], lens)
+    for t in (q, k, v):
+        _fill_rows(t, pads, float("nan"))
+    return ThdBatch("padded_causal", "bf16", h, h, d, cu, cu.copy(), padded, padded.copy(),
+                    padded.copy(), padded.copy(), padded.copy(),
+                    np.full(b, MASK_TOP_LEFT, dtype=np.int8), None, STATS_HEAD_MAJOR,
+                    q, k, v, cap, cap)
+
+
+def mixed_gqa(seed: int = WORKLOAD_SEEDS["mixed_gqa"], sigma: float = 1.35) -> ThdBatch:
+    rng = np.random.default_rng(seed)
+    b, h_q, h_kv, d = 32, 32, 8, 128
+    while True:
+        lens = np.clip(np.round(512.0 * np.exp(sigma * rng.standard_normal(b))), 16, 4096)
+        lens = lens.astype(np.int64)
+        if abs(int(lens.sum()) - 32768) <= 3277:
+            break
+    gaps = rng.integers(0, 8, size=b, endpoint=True)
+    cu = _cumsum0(lens)
+    padded = _cumsum0(lens + gaps)
+    cap = int(padded[-1])
+    q = _normal(rng, (cap, h_q, d), "bf16")
+    k = _normal(rng, (cap, h_kv, d), "bf16")
+    v = _normal(rng, (cap, h_kv, d), "bf16")
+    pads = _pad_rows(cap, padded[:-1], lens)
+    for t in (q, k, v):
+        _fill_rows(t, pads, float("nan"))
+    mask = rng.integers(0, 2, size=b).astype(np.int8)   # Bernoulli(0.5): 0 none, 1 causal
+    return ThdBatch("mixed_gqa", "bf16", h_q, h_kv, d, cu, cu.copy(), padded, padded.copy(),
+                    padded.copy(), padded.copy(), padded.copy(), mask, None, STATS_TOKEN_MAJOR,
+                    q, k, v, cap, cap)
+
+
+def cp_chunks(seed: int = WORKLOAD_SEEDS["cp_chunks"], docs: int = 2, k_len: int = 65536,
+              q_len: int = 4096, h: int = 16, d: int = 128) -> ThdBatch:
+    rng = np.random.default_rng(seed)
+    cu_k = _cumsum0([k_len] * docs)
+    cu_q = _cumsum0([q_len] * docs)
+    q = _normal(rng, (docs * q_len, h, d), "bf16")
+    k = _normal(rng, (docs * k_len, h, d), "bf16")
+    v = _normal(rng, (docs * k_len, h, d), "bf16")
+    qco = np.full(docs, k_len - q_len, dtype=np.int32)
+    return ThdBatch("cp_chunks", "bf16", h, h, d, cu_q, cu_k, cu_q.copy(), cu_k.copy(),
+                    cu_k.copy(), cu_q.copy(), cu_q.copy(),
+                    np.full(docs, MASK_BOTTOM_RIGHT, dtype=np.int8), qco, STATS_HEAD_MAJOR,
+                    q, k, v, docs * q_len, docs * q_len)
+
+
+def separate_padding(seed: int = WORKLOAD_SEEDS["separate_padding"], b: int = 64,
+                     max_len: int = 4096, h: int = 32, d: int = 64, q_multiple: int = 64) -> ThdBatch:
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, max_len, size=b, endpoint=True)
+    lens[int(rng.integers(0, b))] = 0
+    cu = _cumsum0(lens)
+    q_slots = (lens + q_multiple - 1) // q_multiple * q_multiple
+    off_q = _cumsum0(q_slots)
+    off_k = _cumsum0(lens + 1)            # one identifier row after each sequence
+    cap_q, cap_k = int(off_q[-1]), int(off_k[-1])
+    q = _normal(rng, (cap_q, h, d), "fp16")
+    k = _normal(rng, (cap_k, h, d), "fp16")
+    v = _normal(rng, (cap_k, h, d), "fp16")
+    _fill_rows(q, _pad_rows(cap_q, off_q[:-1], lens), float("nan"))
+    mask = rng.integers(0, 3, size=b).astype(np.int8)
+    return ThdBatch("separate_padding", "fp16", h, h, d, cu, cu.copy(), off_q, off_k,
+                    off_k.copy(), off_q.copy(), off_q.copy(), mask, None, STATS_TOKEN_MAJOR,
+                    q, k, v, cap_q, cap_q)
+
+
+WORKLOADS = {"tiny_padded": tiny_padded, "padded_causal": padded_causal,
+             "mixed_gqa": mixed_gqa, "cp_chunks": cp_chunks,
+             "separate_padding": separate_padding}
+
+
+def make(name: str, seed: int | None = None, **kw) -> ThdBatch:
+    fn = WORKLOADS[name]
+    return fn(**kw) if seed is None else fn(seed=seed, **kw)
+
+
+def random_pack(seed: int, *, batch: int = 4, max_len: int = 200, h_q: int = 4, h_kv: int = 2,
+                d: int = 64, dtype: str = "bf16", max_gap: int = 9, stats_layout: int | None = None,
+                masks=(0, 1, 2), with_qco: bool | None = None, allow_empty: bool = True,
+                separate_kv_len: bool = True, nan_pads: bool = True) -> ThdBatch:
+    """Small random pack for fuzzing: ragged lengths, per-tensor gaps, mixed masks.
+
+    Q/O/Stats share one set of offsets and K/V another, each with its own random
+    gaps; query and key lengths differ per sequence when ``separate_kv_len``.
+    """
+    rng = np.random.default_rng(seed)
+    lo = 0 if allow_empty else 1
+    lq = rng.integers(lo, max_len, size=batch, endpoint=True)
+    lk = rng.integers(lo, max_len, size=batch, endpoint=True) if separate_kv_len else lq.copy()
+    gq = rng.integers(0, max_gap, size=batch, endpoint=True)
+    gk = rng.integers(0, max_gap, size=batch, endpoint=True)
+    lead_q, lead_k = int(rng.integers(0, 4)), int(rng.integers(0, 4))
+    off_q = (_cumsum0(lq + gq) + lead_q).astype(np.int32)
+    off_k = (_cumsum0(lk + gk) + lead_k).astype(np.int32)
+    cap_q, cap_k = int(off_q[-1]) + int(rng.integers(0, 3)), int(off_k[-1]) + int(rng.integers(0, 3))
+    q = _normal(rng, (cap_q, h_q, d), dtype)
+    k = _normal(rng, (cap_k, h_kv, d), dtype)
+    v = _normal(rng, (cap_k, h_kv, d), dtype)
+    if nan_pads:
+        _fill_rows(q, _pad_rows(cap_q, off_q[:-1], lq), float("nan"))
+        pk = _pad_rows(cap_k, off_k[:-1], lk)
+        _fill_rows(k, pk, float("nan"))
+        _fill_rows(v, pk, float("nan"))
+    mask = rng.choice(np.array(masks, dtype=np.int8), size=batch)
+    if with_qco is None:
+        with_qco = bool(rng.integers(0, 2))
+    qco = None
+    if with_qco:
+        # any shift from "all rows dead" to "all keys visible"
+        qco = np.array([int(rng.integers(-int(a) - 2, int(b_) + 2)) for a, b_ in zip(lq, lk)],
+                       dtype=np.int32)
+    if stats_layout is None:
+        stats_layout = int(rng.integers(0, 2))
+    return ThdBatch(f"random_pack_{seed}", dtype, h_q, h_kv, d, _cumsum0(lq), _cumsum0(lk),
+                    off_q, off_k, off_k.copy(), off_q.copy(), off_q.copy(), mask, qco,
+                    stats_layout, q, k, v, cap_q, cap_q)
