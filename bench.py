@@ -1,0 +1,403 @@
+"""Benchmark: packed-THD attention forward on one GB300 (or N weak-scaled replicas).
+
+Default workload: long-context context-parallel query chunks -- 2 documents of
+65536 keys, a 4096-row query chunk per document at causal offset k_len - q_len
+(bottom-right causal), h_q = h_kv = 16, d = 128, bf16, head-major LSE. One step
+is one ``thd_attn_fwd`` (setup kernel + attention kernel) over that batch.
+
+Metric: TFLOP/s counted over unmasked score entries, 4 * d * N_visible (QK^T and
+PV, multiply-add = 2), summed over sequences and query heads.
+
+``--impl reference`` times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed-THD attn fwd TFLOP/s (unmasked FLOPs) and % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD_DESC = {
+    "cp_chunks": "long-context CP chunks: 2 docs x 65536 K rows (131072 K/V tokens), one 4096-row Q chunk "
+                 "per doc at q_causal_offset = k_len - q_len (bottom-right causal), h_q=h_kv=16, d=128, "
+                 "bf16, packed K/V, head-major LSE",
+    "mixed_gqa": "mixed-policy GQA pack: 32 seqs lognormal lens (median 512) ~32k tokens, h_q=32 h_kv=8, "
+                 "d=128, bf16, per-seq causal ~ Bernoulli(0.5), 0-8 pad rows, token-major LSE",
+    "separate_padding": "separate Q/O vs K/V padding: 64 seqs lens U[0,4096], Q/O padded to 64, K/V 1-row gaps, "
+                        "h=32, d=64, fp16, masks {none, TL, BR}, token-major LSE",
+    "padded_causal": "padded THD causal: 8 seqs lens U[64,1024], 0-16 pad rows, h=16, d=128, bf16, head-major LSE",
+}
+
+
+def unmasked_entries(batch) -> int:
+    """Visible (row, key) pairs summed over sequences and query heads."""
+    lq, lk = batch.lens_q(), batch.lens_k()
+    total = 0
+    for b in range(batch.batch):
+        mt = int(batch.mask_type[b])
+        if mt == 0:
+            total += int(lq[b]) * int(lk[b])
+            continue
+        shift = 0 if mt == 1 else (int(lk[b] - lq[b]) if batch.q_causal_offset is None
+                                   else int(batch.q_causal_offset[b]))
+        i = np.arange(int(lq[b]), dtype=np.int64)
+        total += int(np.clip(i + shift + 1, 0, int(lk[b])).sum())
+    return total * batch.h_q
+
+
+def valid_bytes(batch) -> int:
+    """Algorithmic HBM bytes: valid Q/K/V/O rows once, plus the LSE values."""
+    e = batch.q.element_size()
+    tq, tk = int(batch.lens_q().sum()), int(batch.lens_k().sum())
+    return (2 * tq * batch.h_q * batch.d + 2 * tk * batch.h_kv * batch.d) * e + 4 * tq * batch.h_q
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def barrier(dist, device):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+
+
+def max_over_ranks(dist, x: float, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample_time(batch, budget_s: float, max_rows: int | None = None):
+    """Run the oracle on row slices of the workload until ``budget_s`` elapses.
+
+    Returns (seconds, unmasked FLOPs computed, description)."""
+    from oracle import attention_one_head, causal_shift
+    q = batch.q
+    scale = 1.0 / math.sqrt(batch.d) if batch.softmax_scale is None else batch.softmax_scale
+    lq, lk = batch.lens_q(), batch.lens_k()
+    group = batch.h_q // batch.h_kv
+    rows_per_call = 64
+    flops = 0
+    done = []
+    t0 = time.perf_counter()
+    stop = False
+    for b in range(batch.batch):
+        if stop:
+            break
+        shift = causal_shift(int(batch.mask_type[b]), int(lq[b]), int(lk[b]),
+                             None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+        for r0 in range(0, int(lq[b]), rows_per_call):
+            r1 = min(int(lq[b]), r0 + rows_per_call)
+            for h in range(batch.h_q):
+                g = h // group
+                qb = q[batch.off_q[b]:batch.off_q[b] + lq[b], h].to(torch.float64).numpy()
+                kb = batch.k[batch.off_k[b]:batch.off_k[b] + lk[b], g].to(torch.float64).numpy()
+                vb = batch.v[batch.off_v[b]:batch.off_v[b] + lk[b], g].to(torch.float64).numpy()
+                ts = time.perf_counter()
+                attention_one_head(qb, kb, vb, scale, shift, rows=slice(r0, r1))
+                t_step = time.perf_counter() - ts
+                i = np.arange(r0, r1, dtype=np.int64)
+                n = (r1 - r0) * int(lk[b]) if shift is None else int(np.clip(i + shift + 1, 0, int(lk[b])).sum())
+                flops += 4 * batch.d * n
+                done.append(t_step)
+                if sum(done) >= budget_s or (max_rows is not None and len(done) * rows_per_call >= max_rows):
+                    stop = True
+                    break
+            if stop:
+                break
+    secs = sum(done)
+    desc = (f"{len(done)} (row-slice x head) oracle calls of {rows_per_call} query rows each, "
+            f"starting at row 0 of sequence 0, float64 numpy; conversion of inputs excluded")
+    return secs, flops, desc
+
+
+def run_reference(args, batch):
+    """CPU oracle timed on the host cores over a bounded sample per step."""
+    dist, rank, world, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    per_step_budget = args.ref_step_seconds
+    for _ in range(args.warmup):
+        oracle_sample_time(batch, per_step_budget / 4)
+    times, flops = [], []
+    desc = ""
+    for _ in range(args.steps):
+        s, f, desc = oracle_sample_time(batch, per_step_budget)
+        times.append(s)
+        flops.append(f)
+    total_s, total_f = sum(times), sum(flops)
+    value = total_f / total_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(args, batch),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}; budget {per_step_budget:.1f} s"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(args, batch):
+    return {"workload": WORKLOAD_DESC.get(args.workload, args.workload), "name": args.workload,
+            "batch": batch.batch, "h_q": batch.h_q, "h_kv": batch.h_kv, "d": batch.d,
+            "tokens_q": int(batch.lens_q().sum()), "tokens_k": int(batch.lens_k().sum()),
+            "unmasked_entries": unmasked_entries(batch),
+            "l2": "inputs larger than L2 (K/V alone exceed 129 MB); no flush between steps"
+            if valid_bytes(batch) > 129e6 else "inputs smaller than L2; L2 flushed between timed steps",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cp_chunks")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=0.5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from ragged_varlen_attention_gb300 import workloads as wl
+    batch = wl.make(args.workload)
+    if args.impl == "reference":
+        run_reference(args, batch)
+        return
+
+    from ragged_varlen_attention_gb300 import binding as bd
+    from ragged_varlen_attention_gb300 import build
+    dist, rank, world, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0 or not os.path.exists(bd.library_path()):
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    kernel = {"auto": bd.KERNEL_AUTO, "simt": bd.KERNEL_SIMT, "tcgen05": bd.KERNEL_TCGEN05}[args.kernel]
+
+    # host (pinned) inputs and device copies
+    ints = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt))
+    host = {"q": batch.q.pin_memory(), "k": batch.k.pin_memory(), "v": batch.v.pin_memory(),
+            "cu_q": ints(batch.cu_seqlens_q).pin_memory(), "cu_k": ints(batch.cu_seqlens_kv).pin_memory(),
+            "offs": [ints(x).pin_memory() for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o,
+                                                    batch.off_s)],
+            "mask": ints(batch.mask_type, np.int8).pin_memory(),
+            "qco": None if batch.q_causal_offset is None else ints(batch.q_causal_offset).pin_memory()}
+    dev = {k: (None if v is None else ([t.to(device) for t in v] if isinstance(v, list) else v.to(device)))
+           for k, v in host.items()}
+    o = torch.zeros((batch.cap_o, batch.h_q, batch.d), dtype=batch.torch_dtype, device=device)
+    stats = torch.zeros((batch.stats_numel,), dtype=torch.float32, device=device)
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    stats_host = torch.empty(stats.shape, dtype=stats.dtype).pin_memory()
+    plan = bd.plan_for_tensors(dev["q"], dev["k"], dev["v"], o, batch.batch, batch.cap_s,
+                               batch.stats_layout, batch.softmax_scale, kernel)
+    ws = bd.alloc_workspace(plan, device)
+    stream = torch.cuda.current_stream(device)
+    small_inputs = valid_bytes(batch) <= 129e6
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device) if small_inputs else None
+
+    def step():
+        bd.thd_attn_fwd(plan, dev["q"], dev["k"], dev["v"], o, stats, dev["cu_q"], dev["cu_k"], *dev["offs"],
+                        dev["mask"], dev["qco"], ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    status = bd.thd_attn_read_status(plan, ws, stream)
+    if status != 0:
+        raise SystemExit(f"device status word {status:#x} on the benchmark workload")
+
+    flop_per_step = 4 * batch.d * unmasked_entries(batch)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    sampler = ClockSampler(gpu_index)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bd.profile_enable(plan, args.steps)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(dist, device)
+    if flush is None:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier(dist, device)
+        total_ms = ev0.elapsed_time(ev1)
+    else:
+        # L2 flushed between steps; only the fwd calls are inside the timed events
+        total_ms = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1)
+            ev0.record(stream)
+            step()
+            ev1.record(stream)
+            ev1.synchronize()
+            total_ms += ev0.elapsed_time(ev1)
+        barrier(dist, device)
+    clocks = sampler.stop()
+    kernel_ms, kernel_launches = bd.profile_read(plan)
+    bd.profile_enable(plan, 0)
+    ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
+    value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+    # end-to-end through the public API: pinned host inputs -> device -> fwd -> host outputs
+    h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"], host["cu_q"],
+                                                      host["cu_k"], host["mask"], *host["offs"]))
+    if host["qco"] is not None:
+        h2d += host["qco"].numel() * host["qco"].element_size()
+    d2h = o_host.numel() * o_host.element_size() + stats_host.numel() * 4
+
+    def e2e_step():
+        for name in ("q", "k", "v", "cu_q", "cu_k", "mask", "qco"):
+            if host[name] is not None:
+                dev[name].copy_(host[name], non_blocking=True)
+        for dt, ht in zip(dev["offs"], host["offs"]):
+            dt.copy_(ht, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+        stats_host.copy_(stats, non_blocking=True)
+
+    e2e_step()
+    barrier(dist, device)
+    ev0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    barrier(dist, device)
+    e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / args.e2e_steps, device)
+    e2e_value = flop_per_step * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    kernel_tflops = flop_per_step / (kernel_ms * 1e-3) / 1e12 if kernel_ms > 0 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if batch.dtype == "bf16" else batch.dtype, "data": "synthetic",
+        "config": {**config_block(args, batch),
+                   "kernel": "tcgen05" if plan.kernel == bd.KERNEL_TCGEN05 else "simt",
+                   "flop_per_step": flop_per_step},
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": None if kernel_tflops is None else kernel_tflops / peak,
+                     "peak_source": f"bf16_tflops (burst) of {peak_src} MEASURED_PEAKS.json"
+                     if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                     "kernel": "attention kernel alone (CUDA events on its stream)",
+                     "kernel_ms": kernel_ms, "launches": kernel_launches,
+                     "traffic": None},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": args.e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, flops, desc = oracle_sample_time(batch, args.cpu_baseline_seconds)
+        line["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc + f"; {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

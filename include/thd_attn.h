@@ -160,6 +160,16 @@ void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]);
 
 void thd_attn_plan_destroy(thd_attn_plan_t plan);
 
+/* Kernel timing for benchmarks. After thd_attn_profile_enable(plan, slots > 0),
+ * each thd_attn_fwd on this plan records a CUDA event pair around the attention
+ * kernel alone (not the setup kernel) on its stream, for up to `slots` calls.
+ * thd_attn_profile_read waits for the recorded events, returns the mean
+ * attention-kernel time in milliseconds and the number of launches it covers,
+ * and starts a new recording. slots = 0 turns recording off. Not for use while
+ * a stream is being captured into a CUDA graph. */
+thd_status_t thd_attn_profile_enable(thd_attn_plan_t plan, int32_t slots);
+thd_status_t thd_attn_profile_read(thd_attn_plan_t plan, float* mean_ms, int32_t* launches);
+
 const char* thd_attn_status_string(thd_status_t status);
 
 /* All-axes span in bytes of a strided view: ((rows-1)*s_t + (heads-1)*s_h + (d-1) + 1) * elem,

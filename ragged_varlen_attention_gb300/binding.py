@@ -50,7 +50,8 @@ class ThdAttnDesc(ctypes.Structure):
 _LIB = None
 _EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_plan_kernel",
             "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
-            "thd_attn_status_string", "thd_attn_view_span_bytes"]
+            "thd_attn_status_string", "thd_attn_view_span_bytes", "thd_attn_profile_enable",
+            "thd_attn_profile_read"]
 
 
 def library_path() -> str:
@@ -86,6 +87,10 @@ def load_library():
     lib.thd_attn_status_string.restype = ctypes.c_char_p
     lib.thd_attn_view_span_bytes.argtypes = [ctypes.c_int64] * 6
     lib.thd_attn_view_span_bytes.restype = ctypes.c_int64
+    lib.thd_attn_profile_enable.argtypes = [vp, ctypes.c_int32]
+    lib.thd_attn_profile_enable.restype = ctypes.c_int
+    lib.thd_attn_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32p]
+    lib.thd_attn_profile_read.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -188,6 +193,23 @@ def thd_attn_read_status(plan: ThdAttnPlan, workspace, stream=None) -> int:
     if st != 0:
         raise ThdAttnError(st, "thd_attn_read_status")
     return out.value
+
+
+def profile_enable(plan: ThdAttnPlan, slots: int) -> None:
+    """Record CUDA events around the attention kernel of the next ``slots`` fwd calls."""
+    st = load_library().thd_attn_profile_enable(ctypes.c_void_p(plan.handle), int(slots))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_profile_enable")
+
+
+def profile_read(plan: ThdAttnPlan) -> tuple[float, int]:
+    """(mean attention-kernel ms, launches recorded) since ``profile_enable``."""
+    ms, n = ctypes.c_float(), ctypes.c_int32()
+    st = load_library().thd_attn_profile_read(ctypes.c_void_p(plan.handle), ctypes.byref(ms),
+                                              ctypes.byref(n))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_profile_read")
+    return float(ms.value), int(n.value)
 
 
 def alloc_workspace(plan: ThdAttnPlan, device) -> torch.Tensor:

@@ -1,0 +1,315 @@
+// Host side of the C ABI declared in include/thd_attn.h: descriptor validation,
+// capacity checks by the all-axes span rule (cudnn-frontend PR #462, "The fix"),
+// kernel selection, workspace layout, and the asynchronous fwd enqueue.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+#include "tc_launch.h"
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int elem_bytes(thd_dtype_t t) { return t == THD_FP32 ? 4 : 2; }
+
+int num_sms_of_current_device() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+bool tc_applicable(const thd_attn_desc_t& d) {
+  if (!thd::tc_kernel_available()) return false;
+  if (d.dtype != THD_BF16 && d.dtype != THD_FP16) return false;
+  if (d.d != 64 && d.d != 128) return false;
+  const int eb = elem_bytes(d.dtype);
+  for (int i = 0; i < 3; ++i) {  // Q, K, V go through TMA: 16-byte strides, < 2^31 rows
+    if ((d.stride_tok[i] * eb) % 16 != 0 || (d.stride_head[i] * eb) % 16 != 0) return false;
+    if (d.stride_tok[i] <= 0 || d.stride_head[i] <= 0) return false;
+    if (d.cap_rows[i] >= (int64_t(1) << 31)) return false;
+  }
+  if ((d.stride_tok[3] * eb) % 16 != 0 || (d.stride_head[3] * eb) % 16 != 0) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t thd_attn_view_span_bytes(int64_t rows, int64_t heads, int64_t d, int64_t stride_tok,
+                                 int64_t stride_head, int64_t elem) {
+  if (rows <= 0 || heads <= 0 || d <= 0) return 0;
+  return ((rows - 1) * stride_tok + (heads - 1) * stride_head + (d - 1) + 1) * elem;
+}
+
+const char* thd_attn_status_string(thd_status_t s) {
+  switch (s) {
+    case THD_OK: return "THD_OK";
+    case THD_ERR_INVALID_ARG: return "THD_ERR_INVALID_ARG";
+    case THD_ERR_UNSUPPORTED: return "THD_ERR_UNSUPPORTED";
+    case THD_ERR_ALIGNMENT: return "THD_ERR_ALIGNMENT";
+    case THD_ERR_CAPACITY: return "THD_ERR_CAPACITY";
+    case THD_ERR_WORKSPACE: return "THD_ERR_WORKSPACE";
+    case THD_ERR_CUDA: return "THD_ERR_CUDA";
+  }
+  return "THD_ERR_UNKNOWN";
+}
+
+thd_status_t thd_attn_plan(thd_attn_plan_t* out, const thd_attn_desc_t* desc, size_t* ws_bytes) {
+  if (!out || !desc || !ws_bytes) return THD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const thd_attn_desc_t& d = *desc;
+  if (d.dtype != THD_BF16 && d.dtype != THD_FP16 && d.dtype != THD_FP32) return THD_ERR_INVALID_ARG;
+  if (d.batch < 0 || d.h_q < 1 || d.h_kv < 1 || d.h_q % d.h_kv != 0) return THD_ERR_INVALID_ARG;
+  if (d.d < 1) return THD_ERR_INVALID_ARG;
+  if (d.d > 128) return THD_ERR_UNSUPPORTED;
+  if (d.stats_layout != THD_STATS_TOKEN_MAJOR && d.stats_layout != THD_STATS_HEAD_MAJOR)
+    return THD_ERR_INVALID_ARG;
+  if (d.kernel != THD_KERNEL_AUTO && d.kernel != THD_KERNEL_SIMT && d.kernel != THD_KERNEL_TCGEN05)
+    return THD_ERR_INVALID_ARG;
+  if (d.cap_rows_stats < 0 || d.cap_rows_stats >= (int64_t(1) << 31)) return THD_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) {
+    if (d.cap_rows[i] < 0 || d.cap_rows[i] >= (int64_t(1) << 31)) return THD_ERR_INVALID_ARG;
+    if (d.stride_tok[i] < 0 || d.stride_head[i] < 0 || d.bytes[i] < 0) return THD_ERR_INVALID_ARG;
+  }
+  float scale = d.softmax_scale;
+  if (std::isnan(scale)) scale = 1.0f / std::sqrt((float)d.d);
+  if (!std::isfinite(scale)) return THD_ERR_INVALID_ARG;
+
+  // capacity: the all-axes span of each declared view must fit its allocation
+  const int eb = elem_bytes(d.dtype);
+  const int64_t heads[4] = {d.h_q, d.h_kv, d.h_kv, d.h_q};
+  for (int i = 0; i < 4; ++i) {
+    if (d.bytes[i] == 0) continue;
+    const int64_t span =
+        thd_attn_view_span_bytes(d.cap_rows[i], heads[i], d.d, d.stride_tok[i], d.stride_head[i], eb);
+    if (span > d.bytes[i]) return THD_ERR_CAPACITY;
+  }
+
+  thd_kernel_t kernel;
+  if (d.kernel == THD_KERNEL_SIMT) {
+    kernel = THD_KERNEL_SIMT;
+  } else if (d.kernel == THD_KERNEL_TCGEN05) {
+    if (!tc_applicable(d)) return THD_ERR_UNSUPPORTED;
+    kernel = THD_KERNEL_TCGEN05;
+  } else {
+    kernel = tc_applicable(d) ? THD_KERNEL_TCGEN05 : THD_KERNEL_SIMT;
+  }
+
+  auto* p = new (std::nothrow) thd_attn_plan_s;
+  if (!p) return THD_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->desc = d;
+  p->kernel = kernel;
+  p->scale = scale;
+  p->elem_bytes = eb;
+  if (kernel == THD_KERNEL_TCGEN05) {
+    p->rows_per_unit = thd::tc_rows_per_unit();
+    p->keys_per_tile = thd::tc_keys_per_tile();
+  } else {
+    p->rows_per_unit = thd::simt_rows_per_unit(d.d);
+    p->keys_per_tile = thd::kSimtKeysPerTile;
+  }
+  if (d.stats_layout == THD_STATS_TOKEN_MAJOR) {
+    p->stats_tok = d.h_q;
+    p->stats_head = 1;
+  } else {
+    p->stats_tok = 1;
+    p->stats_head = d.cap_rows_stats;
+  }
+  // non-overlapping O rows bound the number of (sequence, query tile) pairs
+  const int64_t max_pairs = (int64_t)d.batch + (d.cap_rows[3] + p->rows_per_unit - 1) / p->rows_per_unit + 1;
+  if (max_pairs * d.h_q >= (int64_t(1) << 31)) {
+    delete p;
+    return THD_ERR_UNSUPPORTED;
+  }
+  p->max_pairs = (int32_t)max_pairs;
+  int64_t off = 0;
+  p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
+  p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
+  p->ws_off[2] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
+  p->ws_off[3] = off; off = align_up(off + max_pairs * (int64_t)sizeof(thd::PairRec), kAlign);
+  p->ws_bytes = (size_t)off;
+  *ws_bytes = p->ws_bytes;
+  *out = p;
+  return THD_OK;
+}
+
+thd_kernel_t thd_attn_plan_kernel(thd_attn_plan_t plan) { return plan ? plan->kernel : THD_KERNEL_AUTO; }
+
+void thd_attn_plan_geometry(thd_attn_plan_t plan, int32_t* rows, int32_t* keys, int32_t* max_pairs) {
+  if (!plan) return;
+  if (rows) *rows = plan->rows_per_unit;
+  if (keys) *keys = plan->keys_per_tile;
+  if (max_pairs) *max_pairs = plan->max_pairs;
+}
+
+void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]) {
+  if (!plan || !offsets) return;
+  for (int i = 0; i < 4; ++i) offsets[i] = plan->ws_off[i];
+}
+
+namespace {
+void profile_release(thd_attn_plan_t plan) {
+  if (plan->prof_events) {
+    for (int i = 0; i < 2 * plan->prof_slots; ++i) cudaEventDestroy(plan->prof_events[i]);
+    delete[] plan->prof_events;
+  }
+  plan->prof_events = nullptr;
+  plan->prof_slots = 0;
+  plan->prof_count = 0;
+}
+}  // namespace
+
+void thd_attn_plan_destroy(thd_attn_plan_t plan) {
+  if (!plan) return;
+  profile_release(plan);
+  delete plan;
+}
+
+thd_status_t thd_attn_profile_enable(thd_attn_plan_t plan, int32_t slots) {
+  if (!plan || slots < 0) return THD_ERR_INVALID_ARG;
+  profile_release(plan);
+  if (slots == 0) return THD_OK;
+  plan->prof_events = new (std::nothrow) cudaEvent_t[2 * slots];
+  if (!plan->prof_events) return THD_ERR_INVALID_ARG;
+  for (int i = 0; i < 2 * slots; ++i) {
+    if (cudaEventCreate(&plan->prof_events[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(plan->prof_events[j]);
+      delete[] plan->prof_events;
+      plan->prof_events = nullptr;
+      return THD_ERR_CUDA;
+    }
+  }
+  plan->prof_slots = slots;
+  plan->prof_count = 0;
+  return THD_OK;
+}
+
+thd_status_t thd_attn_profile_read(thd_attn_plan_t plan, float* mean_ms, int32_t* launches) {
+  if (!plan || !mean_ms || !launches) return THD_ERR_INVALID_ARG;
+  double total = 0.0;
+  const int n = plan->prof_count;
+  for (int i = 0; i < n; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(plan->prof_events[2 * i + 1]) != cudaSuccess) return THD_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms, plan->prof_events[2 * i], plan->prof_events[2 * i + 1]) != cudaSuccess)
+      return THD_ERR_CUDA;
+    total += ms;
+  }
+  *mean_ms = n > 0 ? (float)(total / n) : 0.f;
+  *launches = n;
+  plan->prof_count = 0;
+  return THD_OK;
+}
+
+thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                          float* stats, const int32_t* cu_q, const int32_t* cu_k, const int32_t* off_q,
+                          const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
+                          const int32_t* off_s, const int8_t* mask, const int32_t* qco, void* workspace,
+                          void* stream_ptr) {
+  if (!plan) return THD_ERR_INVALID_ARG;
+  const thd_attn_desc_t& d = plan->desc;
+  if (!workspace) return THD_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return THD_ERR_WORKSPACE;
+  // metadata is always read for every sequence; a tensor pointer may be NULL only
+  // when its view has no rows (nothing can address it then)
+  if (d.batch > 0 && (!cu_q || !cu_k || !off_q || !off_k || !off_v || !off_o || !off_s || !mask))
+    return THD_ERR_INVALID_ARG;
+  const void* tens[4] = {q, k, v, o};
+  for (int i = 0; i < 4; ++i)
+    if (!tens[i] && d.cap_rows[i] > 0) return THD_ERR_INVALID_ARG;
+  if (!stats && d.cap_rows_stats > 0) return THD_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+
+  thd::SetupParams sp;
+  sp.cu_q = cu_q; sp.cu_k = cu_k;
+  sp.off_q = off_q; sp.off_k = off_k; sp.off_v = off_v; sp.off_o = off_o; sp.off_s = off_s;
+  sp.mask = mask; sp.qco = qco;
+  sp.cap_q = d.cap_rows[0]; sp.cap_k = d.cap_rows[1]; sp.cap_v = d.cap_rows[2]; sp.cap_o = d.cap_rows[3];
+  sp.cap_s = d.cap_rows_stats;
+  sp.batch = d.batch;
+  sp.rows_per_unit = plan->rows_per_unit;
+  sp.keys_per_tile = plan->keys_per_tile;
+  sp.max_pairs = plan->max_pairs;
+  sp.h_q = d.h_q;
+  sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
+  sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
+  sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
+  sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
+
+  thd::FwdParams fp;
+  fp.q = q; fp.k = k; fp.v = v; fp.o = o; fp.stats = stats;
+  for (int i = 0; i < 4; ++i) {
+    fp.stride_tok[i] = d.stride_tok[i];
+    fp.stride_head[i] = d.stride_head[i];
+  }
+  fp.stats_tok = plan->stats_tok;
+  fp.stats_head = plan->stats_head;
+  fp.h_q = d.h_q; fp.h_kv = d.h_kv; fp.d = d.d;
+  fp.scale_log2 = plan->scale * 1.4426950408889634f;
+  fp.header = sp.header;
+  fp.counter = sp.header + thd::kHdrCounter;
+  fp.status = sp.header + thd::kHdrStatus;
+  fp.meta = sp.meta;
+  fp.pairs = sp.pairs;
+
+  // a view with no rows has no TMA descriptor: the SIMT kernel serves that call
+  // (it walks any unit size, so the plan's schedule geometry still applies)
+  bool use_tc = plan->kernel == THD_KERNEL_TCGEN05;
+  for (int i = 0; i < 3; ++i)
+    if (d.cap_rows[i] == 0) use_tc = false;
+  if (use_tc) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
+  }
+
+  const int num_sms = num_sms_of_current_device();
+  if (num_sms <= 0) return THD_ERR_CUDA;
+  if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
+  const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
+  if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
+    return THD_ERR_CUDA;
+  cudaError_t err;
+  if (use_tc) {
+    err = thd::launch_fwd_tc(fp, d, plan->max_pairs, num_sms, stream);
+    if (err == cudaErrorNotSupported) return THD_ERR_UNSUPPORTED;
+  } else {
+    err = thd::launch_fwd_simt(fp, d.dtype, plan->rows_per_unit, num_sms, stream);
+  }
+  if (err != cudaSuccess) return THD_ERR_CUDA;
+  if (prof) {
+    if (cudaEventRecord(plan->prof_events[2 * plan->prof_count + 1], stream) != cudaSuccess)
+      return THD_ERR_CUDA;
+    ++plan->prof_count;
+  }
+  return THD_OK;
+}
+
+thd_status_t thd_attn_read_status(thd_attn_plan_t plan, const void* workspace, uint32_t* host_out,
+                                  void* stream_ptr) {
+  if (!plan || !host_out) return THD_ERR_INVALID_ARG;
+  if (!workspace) return THD_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const char* src = static_cast<const char*>(workspace) + plan->ws_off[0] + 4 * thd::kHdrStatus;
+  if (cudaMemcpyAsync(host_out, src, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return THD_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return THD_ERR_CUDA;
+  return THD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// Internal declarations shared by the host API and the kernels of libthd_attn.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "thd_attn.h"
+
+namespace thd {
+
+// Words of the workspace header. The tile counter is word 0 (the persistent
+// scheduler's claim counter); everything after it is sized by the plan.
+enum HeaderWord : int { kHdrCounter = 0, kHdrStatus = 1, kHdrNumPairs = 2, kHdrNumTiles = 3 };
+constexpr int kHeaderBytes = 64;
+
+// Per-sequence record written by the setup kernel. `shift` is the causal shift:
+// query row i sees keys j < len_k with j <= i + shift (mask 0 stores len_k, which
+// lets every key through for any i >= 0).
+struct SeqMeta {
+  int32_t len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift;
+};
+static_assert(sizeof(SeqMeta) == 32, "SeqMeta is 32 bytes");
+
+// A scheduled unit: rows [row0, row0 + rows_per_unit) of sequence b, for every
+// query head (work id w -> pair w / h_q, head w % h_q).
+struct PairRec {
+  int32_t b, row0;
+};
+
+constexpr int kCostBins = 1024;          // LPT buckets of the setup kernel's counting sort
+constexpr int kSetupThreads = 1024;
+
+struct SetupParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* off_q;
+  const int32_t* off_k;
+  const int32_t* off_v;
+  const int32_t* off_o;
+  const int32_t* off_s;
+  const int8_t* mask;
+  const int32_t* qco;       // may be null
+  int64_t cap_q, cap_k, cap_v, cap_o, cap_s;
+  int32_t batch;
+  int32_t rows_per_unit;
+  int32_t keys_per_tile;
+  int32_t max_pairs;
+  int32_t h_q;
+  uint32_t* header;
+  SeqMeta* meta;
+  int32_t* pair_base;       // [batch + 1]
+  PairRec* pairs;           // [max_pairs]
+};
+
+// Arguments common to both attention kernels.
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* stats;
+  int64_t stride_tok[4];    // elements, Q K V O
+  int64_t stride_head[4];
+  int64_t stats_tok, stats_head;
+  int32_t h_q, h_kv, d;
+  float scale_log2;         // softmax_scale * log2(e)
+  const uint32_t* header;
+  uint32_t* counter;
+  uint32_t* status;
+  const SeqMeta* meta;
+  const PairRec* pairs;
+};
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_setup(const SetupParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_simt(const FwdParams& p, thd_dtype_t dtype, int rows_per_unit, int num_sms,
+                            cudaStream_t stream);
+int simt_rows_per_unit(int d);
+constexpr int kSimtKeysPerTile = 32;
+
+}  // namespace thd
+
+struct thd_attn_plan_s {
+  thd_attn_desc_t desc;
+  thd_kernel_t kernel;
+  int32_t rows_per_unit;
+  int32_t keys_per_tile;
+  int32_t max_pairs;
+  float scale;
+  int64_t stats_tok, stats_head;
+  int elem_bytes;
+  size_t ws_bytes;
+  int64_t ws_off[4];        // header, meta, pair_base, pairs
+  // optional attention-kernel timing (thd_attn_profile_enable)
+  int32_t prof_slots;
+  int32_t prof_count;
+  cudaEvent_t* prof_events; // 2 * prof_slots: start, stop pairs
+};

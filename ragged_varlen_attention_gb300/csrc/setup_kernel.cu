@@ -1,0 +1,176 @@
+// Setup kernel: turns the caller's device-resident lengths and per-tensor ragged
+// offsets into per-sequence metadata and a longest-first list of query tiles,
+// with no device-to-host read (cuDNN-frontend issue "THD lowering never reads the
+// bound ragged offsets", section "Proposal: consume the bound offsets on device";
+// TransformerEngine PR #3274 review: avoid GPU-CPU syncs so the call stays graph
+// capturable).
+//
+// One block of 1024 threads:
+//   1. per sequence: lengths from cu_seqlens, offsets read as bound, validation,
+//      causal shift; block scan of the per-sequence tile counts;
+//   2. histogram of tile costs (KV tiles to visit) in kCostBins buckets;
+//   3. descending exclusive scan of the histogram (longest tiles first);
+//   4. scatter of every (sequence, first row) pair to its bucket's next slot.
+// It also zeroes the persistent scheduler's tile counter (header word 0) and
+// writes the status word, pair count and tile count. Invalid sequences get no
+// tiles and set a status bit; their rows are never touched.
+#include "internal.h"
+
+namespace thd {
+
+namespace {
+
+__device__ __forceinline__ int32_t block_inclusive_scan(int32_t x, int32_t* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int32_t r = x + (warp > 0 ? warp_sums[warp - 1] : 0);
+  __syncthreads();  // warp_sums may be reused by the caller's next scan
+  return r;
+}
+
+// number of KV tiles the pair starting at row0 must visit (max over its rows)
+__device__ __forceinline__ int32_t pair_cost(const SeqMeta& m, int32_t row0, int32_t rows_per_unit,
+                                             int32_t keys_per_tile) {
+  const int64_t r_end = min64((int64_t)m.len_q, (int64_t)row0 + rows_per_unit);
+  const int64_t kmax = min64((int64_t)m.len_k, r_end + (int64_t)m.shift);
+  if (kmax <= 0) return 0;
+  return (int32_t)((kmax + keys_per_tile - 1) / keys_per_tile);
+}
+
+__device__ __forceinline__ int32_t find_seq(const int32_t* pair_base, int32_t batch, int32_t e) {
+  // last b with pair_base[b] <= e (pair_base is non-decreasing, pair_base[0] == 0)
+  int32_t lo = 0, hi = batch;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (pair_base[mid] <= e) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
+  __shared__ uint32_t hist[kCostBins];
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  __shared__ uint32_t status_s;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kCostBins; i += blockDim.x) hist[i] = 0;
+  if (tid == 0) { carry = 0; status_s = 0; }
+  __syncthreads();
+
+  // 1. per-sequence metadata and tile counts
+  for (int32_t base = 0; base < p.batch; base += blockDim.x) {
+    const int32_t b = base + tid;
+    int32_t n = 0;
+    if (b < p.batch) {
+      const int32_t lq = p.cu_q[b + 1] - p.cu_q[b];
+      const int32_t lk = p.cu_k[b + 1] - p.cu_k[b];
+      SeqMeta m;
+      m.len_q = lq; m.len_k = lk;
+      m.off_q = p.off_q[b]; m.off_k = p.off_k[b]; m.off_v = p.off_v[b];
+      m.off_o = p.off_o[b]; m.off_s = p.off_s[b];
+      const int mt = (int)p.mask[b];
+      uint32_t bad = 0;
+      if (lq < 0 || lk < 0) bad |= THD_DEV_BAD_LENGTH;
+      if (mt < 0 || mt > 2) bad |= THD_DEV_BAD_MASK;
+      if (!bad) {
+        auto in_cap = [](int32_t off, int32_t len, int64_t cap) {
+          return off >= 0 && (int64_t)off + (int64_t)len <= cap;
+        };
+        if (!in_cap(m.off_q, lq, p.cap_q) || !in_cap(m.off_k, lk, p.cap_k) ||
+            !in_cap(m.off_v, lk, p.cap_v) || !in_cap(m.off_o, lq, p.cap_o) ||
+            !in_cap(m.off_s, lq, p.cap_s))
+          bad |= THD_DEV_BAD_OFFSET;
+      }
+      int64_t shift;
+      if (mt == THD_MASK_NONE) shift = lk;
+      else if (mt == THD_MASK_CAUSAL_TOP_LEFT) shift = 0;
+      else shift = p.qco ? (int64_t)p.qco[b] : (int64_t)lk - (int64_t)lq;
+      // beyond +-2^30 a shift no longer changes which keys are visible
+      shift = max64(-(1ll << 30), min64(1ll << 30, shift));
+      m.shift = (int32_t)shift;
+      if (bad) {
+        atomicOr(&status_s, bad);
+        m.len_q = 0;  // no tiles, rows untouched
+      } else {
+        n = (lq + p.rows_per_unit - 1) / p.rows_per_unit;
+      }
+      p.meta[b] = m;
+    }
+    const int32_t incl = block_inclusive_scan(n, warp_sums);
+    if (b < p.batch) p.pair_base[b] = carry + incl - n;
+    __syncthreads();
+    if (tid == blockDim.x - 1) carry += incl;
+    __syncthreads();
+  }
+  int32_t total = carry;
+  if (tid == 0) p.pair_base[p.batch] = total;
+  if (total > p.max_pairs) {
+    if (tid == 0) atomicOr(&status_s, (uint32_t)THD_DEV_TILE_OVERFLOW);
+    total = 0;
+  }
+  __syncthreads();
+
+  // 2. cost histogram
+  for (int32_t e = tid; e < total; e += blockDim.x) {
+    const int32_t b = find_seq(p.pair_base, p.batch, e);
+    const SeqMeta m = p.meta[b];
+    const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
+    const int32_t c = min(pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile), kCostBins - 1);
+    atomicAdd(&hist[c], 1u);
+  }
+  __syncthreads();
+
+  // 3. exclusive scan from the most expensive bucket down
+  for (int i = tid; i < kCostBins; i += blockDim.x) {
+    // kCostBins == blockDim.x: one bucket per thread
+    const int32_t cnt = (int32_t)hist[kCostBins - 1 - i];
+    const int32_t incl = block_inclusive_scan(cnt, warp_sums);
+    hist[kCostBins - 1 - i] = (uint32_t)(incl - cnt);
+  }
+  __syncthreads();
+
+  // 4. scatter
+  for (int32_t e = tid; e < total; e += blockDim.x) {
+    const int32_t b = find_seq(p.pair_base, p.batch, e);
+    const SeqMeta m = p.meta[b];
+    const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
+    const int32_t c = min(pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile), kCostBins - 1);
+    const uint32_t slot = atomicAdd(&hist[c], 1u);
+    PairRec r;
+    r.b = b; r.row0 = row0;
+    p.pairs[slot] = r;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    p.header[kHdrCounter] = 0u;
+    p.header[kHdrStatus] = status_s;
+    p.header[kHdrNumPairs] = (uint32_t)total;
+    p.header[kHdrNumTiles] = (uint32_t)total * (uint32_t)p.h_q;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_setup(const SetupParams& p, cudaStream_t stream) {
+  static_assert(kCostBins == kSetupThreads, "one histogram bucket per thread in the scan");
+  setup_kernel<<<1, kSetupThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace thd

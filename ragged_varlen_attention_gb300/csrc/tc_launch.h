@@ -1,0 +1,17 @@
+// Interface of the tcgen05 (tensor-core, TMEM, TMA) forward kernel.
+#pragma once
+
+#include "internal.h"
+
+namespace thd {
+
+bool tc_kernel_available();
+int tc_rows_per_unit();   // query rows of one scheduled unit (two 128-row sub-tiles)
+int tc_keys_per_tile();   // keys per KV tile
+// Encodes the TMA descriptors for Q/K/V from the plan's strides and launches the
+// persistent kernel. Returns cudaErrorNotSupported when the descriptors cannot
+// be encoded for these pointers/strides.
+cudaError_t launch_fwd_tc(const FwdParams& p, const thd_attn_desc_t& desc, int max_pairs, int num_sms,
+                          cudaStream_t stream);
+
+}  // namespace thd

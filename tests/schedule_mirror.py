@@ -1,0 +1,62 @@
+"""CPU mirror of the setup kernel's outputs (metadata, pair list, header words).
+
+The setup kernel's contract, restated independently: per sequence
+``(len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift)``; invalid
+sequences (negative length, offset outside capacity, unknown mask) get
+``len_q = 0`` and a status bit; every valid sequence contributes
+``ceil(len_q / rows_per_unit)`` pairs ``(b, row0)``, ordered by descending cost
+(KV tiles to visit, clamped to the bucket count) -- the order inside one cost
+bucket is not fixed.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+COST_BINS = 1024
+BAD_LENGTH, BAD_OFFSET, BAD_MASK, TILE_OVERFLOW = 1, 2, 4, 8
+
+
+def mirror(batch, rows_per_unit: int, keys_per_tile: int, max_pairs: int, caps=None):
+    """Expected (meta [B, 8] int32, pairs list of (b, row0, cost), status, num_pairs)."""
+    lq = batch.lens_q()
+    lk = batch.lens_k()
+    if caps is None:
+        caps = (batch.q.shape[0], batch.k.shape[0], batch.v.shape[0], batch.cap_o, batch.cap_s)
+    cap_q, cap_k, cap_v, cap_o, cap_s = caps
+    meta = np.zeros((batch.batch, 8), dtype=np.int64)
+    status = 0
+    pairs = []
+    for b in range(batch.batch):
+        offs = [int(x[b]) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)]
+        mt = int(batch.mask_type[b])
+        bad = 0
+        if lq[b] < 0 or lk[b] < 0:
+            bad |= BAD_LENGTH
+        if mt not in (0, 1, 2):
+            bad |= BAD_MASK
+        if not bad:
+            lens = (lq[b], lk[b], lk[b], lq[b], lq[b])
+            for off, n, cap in zip(offs, lens, (cap_q, cap_k, cap_v, cap_o, cap_s)):
+                if off < 0 or off + n > cap:
+                    bad |= BAD_OFFSET
+        if mt == 0:
+            shift = int(lk[b])
+        elif mt == 1:
+            shift = 0
+        else:
+            shift = int(lk[b] - lq[b]) if batch.q_causal_offset is None else int(batch.q_causal_offset[b])
+        shift = max(-(1 << 30), min(1 << 30, shift))
+        meta[b] = [0 if bad else lq[b], lk[b], *offs, shift]
+        status |= bad
+        if bad:
+            continue
+        for t in range((int(lq[b]) + rows_per_unit - 1) // rows_per_unit):
+            row0 = t * rows_per_unit
+            r_end = min(int(lq[b]), row0 + rows_per_unit)
+            kmax = min(int(lk[b]), r_end + shift)
+            cost = 0 if kmax <= 0 else (kmax + keys_per_tile - 1) // keys_per_tile
+            pairs.append((b, row0, min(cost, COST_BINS - 1)))
+    if len(pairs) > max_pairs:
+        status |= TILE_OVERFLOW
+        pairs = []
+    return meta.astype(np.int32), pairs, status, len(pairs)

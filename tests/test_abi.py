@@ -1,0 +1,149 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+entry point, validates descriptors on the host, and applies the all-axes span
+rule for capacities."""
+from __future__ import annotations
+
+import ctypes
+import json
+import math
+import os
+import re
+
+import pytest
+import torch
+
+import ragged_varlen_attention_gb300 as rva
+from ragged_varlen_attention_gb300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "thd_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ragged_varlen_attention_gb300 import build
+    build.build()
+    return bd.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(thd_attn_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9, names
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+
+
+def _desc(**kw):
+    base = dict(dtype=torch.bfloat16, batch=2, h_q=4, h_kv=2, d=128, cap_rows=(100, 80, 80, 100),
+                stride_tok=(512, 256, 256, 512), stride_head=(128, 128, 128, 128), nbytes=(0, 0, 0, 0),
+                cap_rows_stats=100, stats_layout=bd.STATS_TOKEN_MAJOR, softmax_scale=None,
+                kernel=bd.KERNEL_AUTO)
+    base.update(kw)
+    return bd.make_desc(**base)
+
+
+def _plan_status(desc):
+    lib = bd.load_library()
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.thd_attn_plan(ctypes.byref(h), ctypes.byref(desc), ctypes.byref(ws))
+    if st == 0:
+        lib.thd_attn_plan_destroy(h)
+    return st, ws.value
+
+
+def test_plan_accepts_valid(lib):
+    st, ws = _plan_status(_desc())
+    assert st == 0 and ws > 0 and ws % 256 == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h_q=3, h_kv=2), 1),
+    (dict(d=0), 1),
+    (dict(d=160), 2),
+    (dict(batch=-1), 1),
+    (dict(cap_rows=(-1, 80, 80, 100)), 1),
+    (dict(stride_tok=(-4, 256, 256, 512)), 1),
+    (dict(stats_layout=5), 1),
+    (dict(softmax_scale=math.inf), 1),
+    (dict(kernel=9), 1),
+    (dict(nbytes=(100 * 512 * 2 - 2, 0, 0, 0)), 4),      # one element short of the span
+])
+def test_plan_rejects(lib, kw, code):
+    st, _ = _plan_status(_desc(**kw))
+    assert st == code
+
+
+def test_plan_capacity_exact_fit(lib):
+    span = (99 * 512 + 3 * 128 + 127 + 1) * 2
+    assert _plan_status(_desc(nbytes=(span, 0, 0, 0)))[0] == 0
+    assert _plan_status(_desc(nbytes=(span - 1, 0, 0, 0)))[0] == 4
+
+
+def test_span_rule_matches_page_closed_forms(lib):
+    """cudnn-frontend PR #462 'The fix': for token-major inputs the all-axes span equals
+    maxT*h_q (softmax_sum) and maxT*h_q*d (dQ_accum); head-major [h, t] stats span
+    h_q*T_s."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "stats_layout.json")))
+    span = lib.thd_attn_view_span_bytes
+    for max_t, h_q, d in [(7, 3, 5), (1024, 16, 128), (7360, 8, 64)]:
+        assert span(max_t, h_q, 1, h_q, 1, 1) == max_t * h_q
+        assert span(max_t, h_q, d, h_q * d, d, 1) == max_t * h_q * d
+    h_q, t = g["h_q"], g["t_capacity"]
+    seq_stride, head_stride, tok_stride, _ = g["head_major_stats_strides"]
+    assert span(t, h_q, 1, tok_stride, head_stride, 4) == seq_stride * 4
+    # the under-sizing the page describes: sizing head-major stats from the token
+    # stride alone (stride 1) misses a factor h_q
+    assert span(t, 1, 1, tok_stride, 0, 4) * h_q == span(t, h_q, 1, tok_stride, head_stride, 4)
+    assert span(0, 4, 4, 16, 4, 2) == 0
+
+
+def test_kernel_selection(lib):
+    p = bd.thd_attn_plan(_desc(dtype=torch.float32))
+    assert p.kernel == bd.KERNEL_SIMT
+    p = bd.thd_attn_plan(_desc(kernel=bd.KERNEL_SIMT))
+    assert p.kernel == bd.KERNEL_SIMT
+    p = bd.thd_attn_plan(_desc(d=96))
+    assert p.kernel == bd.KERNEL_SIMT
+    with pytest.raises(bd.ThdAttnError):
+        bd.thd_attn_plan(_desc(d=96, kernel=bd.KERNEL_TCGEN05))
+    # token stride not a multiple of 16 bytes: no TMA path
+    with pytest.raises(bd.ThdAttnError):
+        bd.thd_attn_plan(_desc(stride_tok=(520 + 4, 256, 256, 512), kernel=bd.KERNEL_TCGEN05))
+
+
+def test_workspace_layout_counter_first(lib):
+    p = bd.thd_attn_plan(_desc(batch=37))
+    hdr, meta, base, pairs = p.workspace_layout
+    assert hdr == 0 and meta >= 64 and base >= meta + 37 * 32 and pairs >= base + 38 * 4
+    assert p.workspace_bytes >= pairs + p.max_pairs * 8
+    assert all(x % 256 == 0 for x in p.workspace_layout)
+    # capacity bound: every sequence may add one partial tile
+    assert p.max_pairs >= 37 + math.ceil(100 / p.rows_per_unit)
+
+
+def test_fwd_rejects_bad_workspace_without_touching_device(lib):
+    p = bd.thd_attn_plan(_desc())
+    nullp = ctypes.c_void_p(0)
+    args = [ctypes.c_void_p(p.handle)] + [ctypes.c_void_p(256)] * 14 + [nullp, nullp]
+    assert lib.thd_attn_fwd(*args) == 5            # workspace NULL
+    args[15] = ctypes.c_void_p(4096 + 8)
+    assert lib.thd_attn_fwd(*args) == 5            # workspace not 256-byte aligned
+    assert lib.thd_attn_fwd(None, *args[1:]) == 1  # no plan
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.thd_attn_status_string(code).decode().startswith("THD_")
+
+
+def test_package_import_does_not_load_library():
+    # importing the package is side-effect free; the binding loads the library lazily
+    assert hasattr(rva, "thd_attn_forward")
