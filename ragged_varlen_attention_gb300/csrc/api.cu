@@ -30,8 +30,9 @@ int num_sms_of_current_device() {
   return cached[dev];
 }
 
-bool tc_applicable(const thd_attn_desc_t& d) {
+bool tc_applicable(const thd_attn_desc_t& d, float scale) {
   if (!thd::tc_kernel_available()) return false;
+  if (!(scale > 0.f)) return false;  // the softmax takes the row max of unscaled scores
   if (d.dtype != THD_BF16 && d.dtype != THD_FP16) return false;
   if (d.d != 64 && d.d != 128) return false;
   const int eb = elem_bytes(d.dtype);
@@ -102,10 +103,10 @@ thd_status_t thd_attn_plan(thd_attn_plan_t* out, const thd_attn_desc_t* desc, si
   if (d.kernel == THD_KERNEL_SIMT) {
     kernel = THD_KERNEL_SIMT;
   } else if (d.kernel == THD_KERNEL_TCGEN05) {
-    if (!tc_applicable(d)) return THD_ERR_UNSUPPORTED;
+    if (!tc_applicable(d, scale)) return THD_ERR_UNSUPPORTED;
     kernel = THD_KERNEL_TCGEN05;
   } else {
-    kernel = tc_applicable(d) ? THD_KERNEL_TCGEN05 : THD_KERNEL_SIMT;
+    kernel = tc_applicable(d, scale) ? THD_KERNEL_TCGEN05 : THD_KERNEL_SIMT;
   }
 
   auto* p = new (std::nothrow) thd_attn_plan_s;

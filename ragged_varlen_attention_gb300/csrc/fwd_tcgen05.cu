@@ -1,12 +1,607 @@
-// tcgen05 forward kernel (placeholder until the tensor-core path lands).
+// Tensor-core forward kernel for sm_103a: TMA-staged Q/K/V tiles, tcgen05.mma
+// into TMEM for S = Q K^T and O += P V, online softmax in fp32 by warps that own
+// one TMEM lane (query row) each.
+//
+// Work unit: 256 query rows (two 128-row sub-tiles) of one sequence and one query
+// head, claimed from the workspace tile counter by a persistent CTA
+// (cudnn-frontend PR #462, "Root cause": tile_id = atomicAdd(counter, 1); retire
+// once tile_id >= num_tiles). Rows are addressed through the caller's ragged
+// offsets as TMA coordinates over the whole [rows, heads, d] view
+// (cuDNN-frontend issue "THD lowering never reads the bound ragged offsets",
+// "Concrete failure": the per-sequence offset enters as a TMA row coordinate).
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-3  softmax of sub-tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax of sub-tile 1
+//   warp  8    TMEM allocation and MMA issue (one thread)
+//   warp  9    scheduler + TMA producer (one thread)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D, 256+2D).
+// P (bf16/fp16, two per 32-bit column) overwrites the first 64 columns of its S.
+//
+// MMA issue order per KV tile j: PV0(j), QK0(j+1), PV1(j), QK1(j+1). The commit
+// that signals S_t(j+1) therefore also covers PV_t(j), so the softmax warps can
+// rescale O_t in place right after S_t(j+1) is ready.
+//
+// Masking is a select (s = visible ? s : -inf), never an added bias, and the V
+// rows of the last KV tile past len_k are zeroed in shared memory before PV:
+// pad rows may hold NaN (the context-parallel padding case of the cuDNN-frontend
+// issue has "no initialization guarantee", and 0 * NaN = NaN). Only rows
+// r < len_q are stored, so pad rows of O and Stats are never written.
+//
+// Every mbarrier wait is bounded (4 s of %globaltimer); on expiry the kernel sets
+// THD_DEV_WAIT_TIMEOUT in the status word, all roles leave their loops, MMAs in
+// flight are drained and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "ptx.cuh"
 #include "tc_launch.h"
 
 namespace thd {
 
-bool tc_kernel_available() { return false; }
-int tc_rows_per_unit() { return 256; }
-int tc_keys_per_tile() { return 128; }
-cudaError_t launch_fwd_tc(const FwdParams&, const thd_attn_desc_t&, int, int, cudaStream_t) {
+namespace {
+
+constexpr int BM = 128;           // query rows per sub-tile (MMA M, TMEM lanes)
+constexpr int BN = 128;           // keys per KV tile
+constexpr int kThreadsTC = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// barrier indices
+enum : int {
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_S_FULL = 4, B_P_FULL = 6, B_O_FULL = 8, B_O_EMPTY = 10,
+  B_SCHED_FULL = 12, B_SCHED_EMPTY = 14, B_FINAL = 16, B_KV = 17
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;               // 128-byte swizzle atoms along d
+  static constexpr int kTileBytes = BN * D * 2;        // a K or V tile; also a Q sub-tile (BM == BN)
+  static constexpr int kStages = D == 128 ? 4 : 8;     // K/V ring depth
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr int kNumBars = B_KV + 2 * kStages;
+  static constexpr int kOffInfo = kOffBar + kNumBars * 8;
+  static constexpr int kOffMisc = kOffInfo + 2 * 64;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kColS = 0;
+  static constexpr int kColO = 256;
+  static_assert(kColO + 2 * D <= 512, "TMEM columns");
+};
+
+struct UnitInfo {
+  uint32_t w;            // work id; >= num_tiles: no more work
+  int32_t b, row0, h, g;
+  int32_t len_k, off_q, off_k, off_v, off_o, off_s, shift;
+  int32_t n_kv[2];       // KV tiles each sub-tile visits
+  int32_t n_rows[2];     // valid query rows of each sub-tile
+};
+static_assert(sizeof(UnitInfo) == 64, "UnitInfo is 64 bytes");
+
+struct Sync {
+  uint32_t bar0;               // shared address of barrier 0
+  volatile int* abort_flag;
+  uint32_t* status;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+  // bounded wait for the phase of `parity` on barrier i; false on abort/timeout
+  __device__ __forceinline__ bool wait(int i, uint32_t parity) const {
+    const uint32_t b = bar(i);
+    if (ptx::mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+      if (ptx::mbar_try_wait(b, parity)) return true;
+      if ((spin & 63u) == 0) {
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicOr(status, (uint32_t)THD_DEV_WAIT_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  // every lane waits; the outcome is made warp-uniform (an abort seen by one lane
+  // stops the whole warp) so the warp never diverges around __syncwarp
+  __device__ __forceinline__ bool wait_warp(int i, uint32_t parity) const {
+    const bool r = wait(i, parity);
+    return __all_sync(0xffffffffu, r);
+  }
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, uint32_t num_tiles) {
+  UnitInfo u;
+  u.w = w;
+  u.b = u.row0 = u.h = u.g = 0;
+  u.len_k = u.off_q = u.off_k = u.off_v = u.off_o = u.off_s = u.shift = 0;
+  u.n_kv[0] = u.n_kv[1] = u.n_rows[0] = u.n_rows[1] = 0;
+  if (w >= num_tiles) return u;
+  const PairRec pr = p.pairs[w / (uint32_t)p.h_q];
+  const SeqMeta m = p.meta[pr.b];
+  u.b = pr.b;
+  u.row0 = pr.row0;
+  u.h = (int)(w % (uint32_t)p.h_q);
+  u.g = u.h / (p.h_q / p.h_kv);
+  u.len_k = m.len_k;
+  u.off_q = m.off_q; u.off_k = m.off_k; u.off_v = m.off_v; u.off_o = m.off_o; u.off_s = m.off_s;
+  u.shift = m.shift;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r_begin = pr.row0 + t * BM;
+    const int rows = max(0, min(BM, m.len_q - r_begin));
+    u.n_rows[t] = rows;
+    int n = 0;
+    if (rows > 0) {
+      const int64_t kmax = min64((int64_t)m.len_k, (int64_t)(r_begin + rows - 1) + m.shift + 1);
+      n = kmax > 0 ? (int)((kmax + BN - 1) / BN) : 0;
+    }
+    u.n_kv[t] = n;
+  }
+  return u;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = Cfg<D>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + C::kOffInfo);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 4);
+  const Sync sy{sbase + (uint32_t)C::kOffBar, abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t num_tiles = p.header[kHdrNumTiles];
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(sy.bar(B_Q_FULL + t), 1);
+      ptx::mbar_init(sy.bar(B_Q_EMPTY + t), 1);
+      ptx::mbar_init(sy.bar(B_S_FULL + t), 1);
+      ptx::mbar_init(sy.bar(B_P_FULL + t), BM);
+      ptx::mbar_init(sy.bar(B_O_FULL + t), 1);
+      ptx::mbar_init(sy.bar(B_O_EMPTY + t), BM);
+      ptx::mbar_init(sy.bar(B_SCHED_FULL + t), 1);
+      ptx::mbar_init(sy.bar(B_SCHED_EMPTY + t), 9);  // MMA warp + 8 softmax warps
+    }
+    ptx::mbar_init(sy.bar(B_FINAL), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(sy.bar(B_KV + s), 1);
+      ptx::mbar_init(sy.bar(B_KV + C::kStages + s), 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------ scheduler + TMA producer
+    if (lane == 0) {
+      uint32_t q_uses[2] = {0, 0};
+      uint32_t kv_it = 0;
+      for (uint32_t it = 0;; ++it) {
+        const int slot = (int)(it & 1u);
+        if (!sy.wait(B_SCHED_EMPTY + slot, ((it >> 1) & 1u) ^ 1u)) break;
+        const uint32_t w = atomicAdd(p.counter, 1u);
+        const UnitInfo u = make_unit(p, w, num_tiles);
+        info[slot] = u;
+        ptx::mbar_arrive(sy.bar(B_SCHED_FULL + slot));
+        if (w >= num_tiles) break;
+        bool ok = true;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || u.n_kv[t] == 0) continue;
+          if (!(ok = sy.wait(B_Q_EMPTY + t, (q_uses[t] & 1u) ^ 1u))) break;
+          ++q_uses[t];
+          const uint32_t qbar = sy.bar(B_Q_FULL + t);
+          ptx::mbar_arrive_expect_tx(qbar, C::kTileBytes);
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            ptx::tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + hf * BM * 128, &tm_q, qbar, hf * 64, u.h,
+                             u.off_q + u.row0 + t * BM);
+        }
+        const int n_tiles = max(u.n_kv[0], u.n_kv[1]);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const int stage = (int)(kv_it % C::kStages);
+            if (!(ok = sy.wait(B_KV + C::kStages + stage, ((kv_it / C::kStages) & 1u) ^ 1u))) break;
+            ++kv_it;
+            const uint32_t fbar = sy.bar(B_KV + stage);
+            ptx::mbar_arrive_expect_tx(fbar, C::kTileBytes);
+            const void* map = kv == 0 ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+            const int row = (kv == 0 ? u.off_k : u.off_v) + j * BN;
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              ptx::tma_load_3d(sbase + C::kOffKV + stage * C::kTileBytes + hf * BN * 128, map, fbar, hf * 64, u.g,
+                               row);
+          }
+        }
+        if (!ok) break;
+      }
+      // loads complete whether or not anyone consumes them; on an abort wait for
+      // the ones still in flight before the CTA may exit
+      if (*abort_flag) {
+        for (int s = 0; s < C::kStages; ++s) {
+          if (kv_it > (uint32_t)s) {
+            const uint32_t last = (kv_it - 1 - (uint32_t)s) / C::kStages * C::kStages + (uint32_t)s;
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(sy.bar(B_KV + s), (last / C::kStages) & 1u) &&
+                   ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+        }
+        for (int t = 0; t < 2; ++t) {
+          if (q_uses[t] == 0) continue;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(sy.bar(B_Q_FULL + t), (q_uses[t] - 1) & 1u) &&
+                 ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // -------------------------------------------------------------- MMA issue
+    constexpr uint32_t kIdescQK = ptx::idesc_f16(BF16, BM, BN, false);
+    constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, BM, D, true);
+    uint32_t q_uses[2] = {0, 0}, p_cnt[2] = {0, 0}, o_uses[2] = {0, 0};
+    uint32_t kv_it = 0;
+    bool issued_any = false;
+    // S_t = Q_t K^T over d: K = 16 per instruction, 4 steps per 128-byte swizzle atom
+    auto issue_qk = [&](int t, int kstage) {
+      const uint32_t qa = sbase + C::kOffQ + t * C::kTileBytes;
+      const uint32_t ka = sbase + C::kOffKV + kstage * C::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)((kk >> 2) * BN * 128 + (kk & 3) * 32);
+        ptx::mma_ss(tmem + C::kColS + t * BN, ptx::sdesc_sw128(qa + off, 16, 1024),
+                    ptx::sdesc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+      }
+    };
+    // O_t += P_t V over keys: K = 16 keys per instruction; P from TMEM (8 columns
+    // per 16 keys), V MN-major (d contiguous): 8-key groups 1024 B apart, 64-wide
+    // d atoms BN*128 B apart
+    auto issue_pv = [&](int t, int vstage, bool accumulate) {
+      const uint32_t va = sbase + C::kOffKV + vstage * C::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        ptx::mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * BN + kk * 8,
+                    ptx::sdesc_sw128(va + kk * 2048, BN * 128, 1024), kIdescPV,
+                    (accumulate || kk > 0) ? 1u : 0u);
+      }
+    };
+    for (uint32_t it = 0;; ++it) {
+      const int slot = (int)(it & 1u);
+      if (!sy.wait_warp(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
+      const UnitInfo u = info[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
+      if (u.w >= num_tiles) break;
+      const int n0 = u.n_kv[0], n1 = u.n_kv[1];
+      const int n_tiles = max(n0, n1);
+      if (n_tiles == 0) continue;
+      const int nt[2] = {n0, n1};
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (ok && nt[t] > 0) ok = sy.wait_warp(B_Q_FULL + t, (q_uses[t]++) & 1u);
+      if (!ok) break;
+      // prologue: S_t(0)
+      int kstage = (int)(kv_it % C::kStages);
+      if (!sy.wait_warp(B_KV + kstage, (kv_it / C::kStages) & 1u)) break;
+      ++kv_it;
+      ptx::tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (nt[t] == 0) continue;
+          issue_qk(t, kstage);
+          ptx::tc_commit(sy.bar(B_S_FULL + t));
+          if (nt[t] == 1) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
+        }
+        ptx::tc_commit(sy.bar(B_KV + C::kStages + kstage));
+        issued_any = true;
+      }
+      __syncwarp();
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int vstage = (int)(kv_it % C::kStages);
+        if (!(ok = sy.wait_warp(B_KV + vstage, (kv_it / C::kStages) & 1u))) break;
+        ++kv_it;
+        if (j == n_tiles - 1 && (j + 1) * BN > u.len_k) {
+          // zero V rows [valid, BN) of the tail tile (whole 128-byte rows: swizzle-agnostic)
+          const int valid = u.len_k - j * BN;
+          const int chunks_per_half = (BN - valid) * 8;
+          uint8_t* vt = smem + C::kOffKV + vstage * C::kTileBytes;
+          for (int idx = lane; idx < chunks_per_half * C::kHalves; idx += 32) {
+            const int hf = idx / chunks_per_half;
+            const int within = idx - hf * chunks_per_half;
+            *reinterpret_cast<uint4*>(vt + hf * BN * 128 + valid * 128 + within * 16) = make_uint4(0, 0, 0, 0);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+        }
+        int knext = -1;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          if (j < nt[t]) {
+            if (j == 0 && !(ok = sy.wait_warp(B_O_EMPTY + t, (o_uses[t]++ & 1u) ^ 1u))) break;
+            if (!(ok = sy.wait_warp(B_P_FULL + t, (p_cnt[t]++) & 1u))) break;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+              issue_pv(t, vstage, j > 0);
+              if (j + 1 == nt[t]) ptx::tc_commit(sy.bar(B_O_FULL + t));
+            }
+            __syncwarp();
+          }
+          if (t == 0 && j + 1 < n_tiles) {
+            knext = (int)(kv_it % C::kStages);
+            if (!(ok = sy.wait_warp(B_KV + knext, (kv_it / C::kStages) & 1u))) break;
+            ++kv_it;
+            ptx::tc_fence_after();
+          }
+          if (j + 1 < nt[t]) {
+            if (lane == 0) {
+              issue_qk(t, knext);
+              ptx::tc_commit(sy.bar(B_S_FULL + t));
+              if (j + 2 == nt[t]) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
+            }
+            __syncwarp();
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (knext >= 0) ptx::tc_commit(sy.bar(B_KV + C::kStages + knext));
+          ptx::tc_commit(sy.bar(B_KV + C::kStages + vstage));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+    // drain every MMA this thread issued before TMEM is released
+    if (lane == 0 && issued_any) {
+      ptx::tc_commit(sy.bar(B_FINAL));
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(sy.bar(B_FINAL), 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int t = warp >> 2;                    // sub-tile
+    const int row = ((warp & 3) << 5) + lane;   // TMEM lane == query row within the sub-tile
+    const uint32_t lane_bits = (uint32_t)((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_bits + (uint32_t)(C::kColS + t * BN);
+    const uint32_t tO = tmem + lane_bits + (uint32_t)(C::kColO + t * D);
+    const float sl2 = p.scale_log2;
+    T* __restrict__ O = static_cast<T*>(p.o);
+    uint32_t s_cnt = 0, o_cnt = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = (int)(it & 1u);
+      if (!sy.wait_warp(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
+      const UnitInfo u = info[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
+      if (u.w >= num_tiles) break;
+      const int nrows = t ? u.n_rows[1] : u.n_rows[0];
+      if (nrows == 0) continue;
+      const int n = t ? u.n_kv[1] : u.n_kv[0];
+      const int r = u.row0 + t * BM + row;      // row inside the sequence
+      const bool live = row < nrows;
+      const int kmax_row = (int)max64(0, min64((int64_t)u.len_k, (int64_t)r + u.shift + 1));
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = sy.wait_warp(B_S_FULL + t, (s_cnt++) & 1u))) break;
+        ptx::tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld(s[c]);
+        const int lim = kmax_row - j * BN;      // columns >= lim are not visible
+        float mx = -INFINITY;
+        if (lim >= BN) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float v = (c * 32 + i < lim) ? __uint_as_float(s[c][i]) : -INFINITY;
+              s[c][i] = __float_as_uint(v);
+              mx = fmaxf(mx, v);
+            }
+        }
+        // reference max in the log2 domain; moved only when the tile max exceeds it
+        // by more than 8 (values of p stay below 2^8), so O is rescaled rarely
+        const float mt = mx * sl2;
+        const bool resc = mt > m + 8.0f;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ptx::ex2(m - mt);
+          m = mt;
+        }
+        l *= alpha;
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        float rs = 0.f;
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {         // keys [64*hp, 64*hp+64) -> P columns [32*hp, 32*hp+32)
+          uint32_t pk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int c = 2 * hp + c2;
+              const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][i]), sl2, -mref));
+              const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][i + 1]), sl2, -mref));
+              rs += p0 + p1;
+              pk[c2 * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
+            }
+          ptx::tmem_st32(tS + 32 * hp, pk);
+        }
+        l += rs;
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // O_t already holds PV of tiles < j (the commit of S_t(j) covered PV_t(j-1))
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + 32 * c, o);
+            ptx::tmem_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st32(tO + 32 * c, o);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sy.bar(B_P_FULL + t));
+      }
+      if (!ok) break;
+      // epilogue: O = O_acc / l on live rows, LSE = (m + log2 l) * ln 2; dead rows 0 / -inf
+      T* orow = O + (int64_t)(u.off_o + r) * p.stride_tok[3] + (int64_t)u.h * p.stride_head[3];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (n > 0) {
+        if (!sy.wait_warp(B_O_FULL + t, (o_cnt++) & 1u)) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + 32 * c, o);
+          ptx::tmem_wait_ld(o);
+          if (live) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sy.bar(B_O_EMPTY + t));
+      } else if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
+      }
+      if (live) {
+        const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994530942f : -INFINITY;
+        p.stats[(int64_t)(u.off_s + r) * p.stats_tok + (int64_t)u.h * p.stats_head] = lse;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// [rows, heads, d] view, box = 64 d-elements x 1 head x 128 rows, 128-byte swizzle;
+// rows past `rows` read as zeros
+bool encode_view(CUtensorMap* map, const void* base, bool bf16, int d, int64_t heads, int64_t rows,
+                 int64_t stride_head, int64_t stride_tok) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)(stride_head * 2), (cuuint64_t)(stride_tok * 2)};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_impl(const FwdParams& p, const thd_attn_desc_t& desc, int max_pairs, int num_sms,
+                        cudaStream_t stream) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!encode_view(&tq, p.q, BF16, D, desc.h_q, desc.cap_rows[0], desc.stride_head[0], desc.stride_tok[0]) ||
+      !encode_view(&tk, p.k, BF16, D, desc.h_kv, desc.cap_rows[1], desc.stride_head[1], desc.stride_tok[1]) ||
+      !encode_view(&tv, p.v, BF16, D, desc.h_kv, desc.cap_rows[2], desc.stride_head[2], desc.stride_tok[2]))
+    return cudaErrorNotSupported;
+  const int smem = C::kSmemBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t max_tiles = (int64_t)max_pairs * desc.h_q;
+  const int grid = (int)max64(1, min64((int64_t)num_sms, max_tiles));
+  fwd_tc_kernel<D, BF16><<<grid, kThreadsTC, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_kernel_available() { return true; }
+int tc_rows_per_unit() { return 2 * BM; }
+int tc_keys_per_tile() { return BN; }
+
+cudaError_t launch_fwd_tc(const FwdParams& p, const thd_attn_desc_t& desc, int max_pairs, int num_sms,
+                          cudaStream_t stream) {
+  const bool bf16 = desc.dtype == THD_BF16;
+  if (desc.d == 128) {
+    return bf16 ? launch_impl<128, true>(p, desc, max_pairs, num_sms, stream)
+                : launch_impl<128, false>(p, desc, max_pairs, num_sms, stream);
+  }
+  if (desc.d == 64) {
+    return bf16 ? launch_impl<64, true>(p, desc, max_pairs, num_sms, stream)
+                : launch_impl<64, false>(p, desc, max_pairs, num_sms, stream);
+  }
   return cudaErrorNotSupported;
 }
 

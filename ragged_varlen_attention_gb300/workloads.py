@@ -140,10 +140,10 @@ def tiny_padded(seed: int = WORKLOAD_SEEDS["tiny_padded"]) -> ThdBatch:
                     STATS_TOKEN_MAJOR, q, k, v, cap, cap)
 
 
-def padded_causal(seed: int = WORKLOAD_SEEDS["padded_causal"]) -> ThdBatch:
+def padded_causal(seed: int = WORKLOAD_SEEDS["padded_causal"], b: int = 8, h: int = 16, d: int = 128,
+                  min_len: int = 64, max_len: int = 1024) -> ThdBatch:
     rng = np.random.default_rng(seed)
-    b, h, d = 8, 16, 128
-    lens = rng.integers(64, 1024, size=b, endpoint=True)
+    lens = rng.integers(min_len, max_len, size=b, endpoint=True)
     gaps = rng.integers(0, 16, size=b, endpoint=True)
     cu = _cumsum0(lens)
     padded = _cumsum0(lens + gaps)
@@ -158,13 +158,14 @@ def padded_causal(seed: int = WORKLOAD_SEEDS["padded_causal"]) -> ThdBatch:
                     q, k, v, cap, cap)
 
 
-def mixed_gqa(seed: int = WORKLOAD_SEEDS["mixed_gqa"], sigma: float = 1.35) -> ThdBatch:
+def mixed_gqa(seed: int = WORKLOAD_SEEDS["mixed_gqa"], sigma: float = 1.35, b: int = 32,
+              median: int = 512, max_len: int = 4096, total: int = 32768, h_q: int = 32,
+              h_kv: int = 8, d: int = 128) -> ThdBatch:
     rng = np.random.default_rng(seed)
-    b, h_q, h_kv, d = 32, 32, 8, 128
     while True:
-        lens = np.clip(np.round(512.0 * np.exp(sigma * rng.standard_normal(b))), 16, 4096)
+        lens = np.clip(np.round(median * np.exp(sigma * rng.standard_normal(b))), 16, max_len)
         lens = lens.astype(np.int64)
-        if abs(int(lens.sum()) - 32768) <= 3277:
+        if abs(int(lens.sum()) - total) <= total // 10:
             break
     gaps = rng.integers(0, 8, size=b, endpoint=True)
     cu = _cumsum0(lens)
