@@ -177,6 +177,35 @@ const char* thd_attn_status_string(thd_status_t status);
 int64_t thd_attn_view_span_bytes(int64_t rows, int64_t heads, int64_t d, int64_t stride_tok,
                                  int64_t stride_head, int64_t elem_bytes);
 
+/* Forward pass without a caller workspace, for callers that cannot allocate
+ * device memory where they run attention (inside a stream being captured into
+ * a CUDA graph, in plugins whose host runtime owns all device memory, or in
+ * serving loops that cannot afford an allocator's implicit synchronisation).
+ * No counterpart exists in the pages this library follows; it is an addition
+ * for such callers.
+ *
+ * Same arguments and results as thd_attn_fwd minus `workspace`. The scratch is a
+ * static device array of thd_attn_static_workspace_capacity() bytes (1 MiB) that
+ * each GPU loading this library keeps until the process exits. The call makes no
+ * allocation of any kind. Returns THD_ERR_WORKSPACE when the plan's
+ * workspace_bytes exceed that capacity.
+ *
+ * The first call on each device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress; make it before any stream capture.
+ * All calls on a device share the array, which keeps the previous call's
+ * contents (each call rewrites what it reads before reading it). Calls that
+ * overlap on the GPU -- e.g. on unordered streams -- race on the array. The
+ * device status word of these calls lives in that array and is not exposed. */
+thd_status_t thd_attn_fwd_static_ws(thd_attn_plan_t plan, const void* q, const void* k, const void* v,
+                                    void* o, float* stats, const int32_t* cu_seqlens_q,
+                                    const int32_t* cu_seqlens_kv, const int32_t* off_q,
+                                    const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
+                                    const int32_t* off_s, const int8_t* mask_type,
+                                    const int32_t* q_causal_offset, void* stream);
+
+/* Capacity in bytes of the static scratch array used by thd_attn_fwd_static_ws. */
+size_t thd_attn_static_workspace_capacity(void);
+
 #ifdef __cplusplus
 }
 #endif

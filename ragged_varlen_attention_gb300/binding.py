@@ -51,7 +51,7 @@ _LIB = None
 _EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_plan_kernel",
             "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
             "thd_attn_status_string", "thd_attn_view_span_bytes", "thd_attn_profile_enable",
-            "thd_attn_profile_read"]
+            "thd_attn_profile_read", "thd_attn_fwd_static_ws", "thd_attn_static_workspace_capacity"]
 
 
 def library_path() -> str:
@@ -91,6 +91,10 @@ def load_library():
     lib.thd_attn_profile_enable.restype = ctypes.c_int
     lib.thd_attn_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32p]
     lib.thd_attn_profile_read.restype = ctypes.c_int
+    lib.thd_attn_fwd_static_ws.argtypes = [vp] * 16
+    lib.thd_attn_fwd_static_ws.restype = ctypes.c_int
+    lib.thd_attn_static_workspace_capacity.argtypes = []
+    lib.thd_attn_static_workspace_capacity.restype = ctypes.c_size_t
     _LIB = lib
     return lib
 
@@ -183,6 +187,24 @@ def thd_attn_fwd(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_
                           _ptr(q_causal_offset), _ptr(workspace), _stream_handle(stream))
     if st != 0:
         raise ThdAttnError(st, "thd_attn_fwd")
+
+
+def thd_attn_fwd_static_ws(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q,
+                           off_k, off_v, off_o, off_s, mask_type, q_causal_offset, stream=None) -> None:
+    """Enqueue the forward pass with the library's static scratch array instead of a
+    caller workspace (see ``thd_attn_fwd_static_ws`` in include/thd_attn.h): for
+    callers that cannot allocate device memory where they run attention."""
+    lib = load_library()
+    st = lib.thd_attn_fwd_static_ws(ctypes.c_void_p(plan.handle), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(stats), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(off_q),
+                                    _ptr(off_k), _ptr(off_v), _ptr(off_o), _ptr(off_s), _ptr(mask_type),
+                                    _ptr(q_causal_offset), _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_fwd_static_ws")
+
+
+def static_workspace_capacity() -> int:
+    return int(load_library().thd_attn_static_workspace_capacity())
 
 
 def thd_attn_read_status(plan: ThdAttnPlan, workspace, stream=None) -> int:
