@@ -61,8 +61,9 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdParams p, int row
     const uint32_t w = work_s;
     __syncthreads();
     if (w >= num_tiles) break;
-    const PairRec pr = p.pairs[w / (uint32_t)p.h_q];
-    const int h = (int)(w % (uint32_t)p.h_q);
+    int pair_idx, h;
+    work_to_unit(p.header, w, p.h_q, p.h_kv, pair_idx, h);
+    const PairRec pr = p.pairs[pair_idx];
     const int g = h / group;
     const SeqMeta m = p.meta[pr.b];
     for (int sub = 0; sub < rows_per_unit; sub += ROWS) {

@@ -10,17 +10,21 @@
 // (cuDNN-frontend issue "THD lowering never reads the bound ragged offsets",
 // "Concrete failure": the per-sequence offset enters as a TMA row coordinate).
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warps 0-3  softmax of sub-tile 0 (thread = query row = TMEM lane)
-//   warps 4-7  softmax of sub-tile 1
-//   warp  8    TMEM allocation and MMA issue (one thread)
-//   warp  9    scheduler + TMA producer (one thread)
+// Warp roles (384 threads = 3 warpgroups, one CTA per SM):
+//   warps 0-3   softmax of sub-tile 0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax of sub-tile 1
+//   warp  8     TMEM allocation / release
+//   warp  9     scheduler + TMA producer (one thread)
+//   warp  10    MMA issue (one thread); warp 11 idle
+// The third warpgroup gives registers back (setmaxnreg) so each softmax thread can
+// hold a full 128-column row of S without spilling.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D, 256+2D).
 // P (bf16/fp16, two per 32-bit column) overwrites the first 64 columns of its S.
 //
-// MMA issue order per KV tile j: PV0(j), QK0(j+1), PV1(j), QK1(j+1). The commit
-// that signals S_t(j+1) therefore also covers PV_t(j), so the softmax warps can
-// rescale O_t in place right after S_t(j+1) is ready.
+// The issuing thread orders MMAs PV0(j), QK0(j+1), PV1(j), QK1(j+1): the two
+// sub-tiles alternate on the tensor core, and each softmax runs while the other
+// sub-tile's MMAs execute. The commit that signals S_t(j+1) also covers PV_t(j),
+// so O_t can be rescaled in place as soon as S_t(j+1) is ready.
 //
 // Masking is a select (s = visible ? s : -inf), never an added bias, and the V
 // rows of the last KV tile past len_k are zeroed in shared memory before PV:
@@ -47,22 +51,30 @@ namespace {
 
 constexpr int BM = 128;           // query rows per sub-tile (MMA M, TMEM lanes)
 constexpr int BN = 128;           // keys per KV tile
-constexpr int kThreadsTC = 320;
-constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
+constexpr int kThreadsTC = 384;
+// launch budget 168 registers/thread (384 x 168 = 64512); warpgroup 2 (MMA, TMA,
+// idle warps) drops to 136 and the two softmax warpgroups rise to 184:
+// 128 x (2 x 184 + 136) = 64512, so every increase can be granted
+constexpr int kRegsSoftmax = 184;
+constexpr int kRegsControl = 136;
+static_assert(2 * kRegsSoftmax + kRegsControl <= 3 * 168, "register split exceeds the launch budget");
+constexpr int kAllocWarp = 8;   // TMEM allocation / release
+constexpr int kTmaWarp = 9;     // scheduler + TMA producer
+constexpr int kIssueWarp = 10;  // MMA issue (one thread)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // barrier indices
 enum : int {
-  B_Q_FULL = 0, B_Q_EMPTY = 2, B_S_FULL = 4, B_P_FULL = 6, B_O_FULL = 8, B_O_EMPTY = 10,
-  B_SCHED_FULL = 12, B_SCHED_EMPTY = 14, B_FINAL = 16, B_KV = 17
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_S_FULL = 4, B_O_FULL = 6, B_SCHED_FULL = 8, B_SCHED_EMPTY = 10,
+  B_FINAL = 12, B_P_DONE = 14, B_O_READ = 16,
+  B_KV = 18  // then kStages "full" and kStages "empty" barriers
 };
 
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;               // 128-byte swizzle atoms along d
   static constexpr int kTileBytes = BN * D * 2;        // a K or V tile; also a Q sub-tile (BM == BN)
-  static constexpr int kStages = D == 128 ? 4 : 8;     // K/V ring depth
+  static constexpr int kStages = D == 128 ? 5 : 10;    // K/V ring depth (fills 224 KB with Q)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
@@ -92,22 +104,24 @@ struct Sync {
   // bounded wait for the phase of `parity` on barrier i; false on abort/timeout
   __device__ __forceinline__ bool wait(int i, uint32_t parity) const {
     const uint32_t b = bar(i);
-    if (ptx::mbar_try_wait(b, parity)) return true;
+    // short spin of non-blocking probes (wake-up latency matters on the critical
+    // path), then sleep-hinted blocking tries so long waits leave the issue slots
+    // to other warps
+    for (int k = 0; k < 96; ++k)
+      if (ptx::mbar_test_wait(b, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
-    for (uint32_t spin = 1;; ++spin) {
-      if (ptx::mbar_try_wait(b, parity)) return true;
-      if ((spin & 63u) == 0) {
-        if (*abort_flag) return false;
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-          *abort_flag = 1;
-          atomicOr(status, (uint32_t)THD_DEV_WAIT_TIMEOUT);
-          return false;
-        }
+    for (;;) {
+      if (ptx::mbar_try_wait_sleep(b, parity, 20000u)) return true;
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, (uint32_t)THD_DEV_WAIT_TIMEOUT);
+        return false;
       }
     }
   }
   // every lane waits; the outcome is made warp-uniform (an abort seen by one lane
-  // stops the whole warp) so the warp never diverges around __syncwarp
+  // stops the whole warp) so the warp never diverges around a warp-wide operation
   __device__ __forceinline__ bool wait_warp(int i, uint32_t parity) const {
     const bool r = wait(i, parity);
     return __all_sync(0xffffffffu, r);
@@ -132,11 +146,13 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
   u.len_k = u.off_q = u.off_k = u.off_v = u.off_o = u.off_s = u.shift = 0;
   u.n_kv[0] = u.n_kv[1] = u.n_rows[0] = u.n_rows[1] = 0;
   if (w >= num_tiles) return u;
-  const PairRec pr = p.pairs[w / (uint32_t)p.h_q];
+  int pair_idx, head;
+  work_to_unit(p.header, w, p.h_q, p.h_kv, pair_idx, head);
+  const PairRec pr = p.pairs[pair_idx];
   const SeqMeta m = p.meta[pr.b];
   u.b = pr.b;
   u.row0 = pr.row0;
-  u.h = (int)(w % (uint32_t)p.h_q);
+  u.h = head;
   u.g = u.h / (p.h_q / p.h_kv);
   u.len_k = m.len_k;
   u.off_q = m.off_q; u.off_k = m.off_k; u.off_v = m.off_v; u.off_o = m.off_o; u.off_s = m.off_s;
@@ -179,13 +195,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       ptx::mbar_init(sy.bar(B_Q_FULL + t), 1);
       ptx::mbar_init(sy.bar(B_Q_EMPTY + t), 1);
       ptx::mbar_init(sy.bar(B_S_FULL + t), 1);
-      ptx::mbar_init(sy.bar(B_P_FULL + t), BM);
       ptx::mbar_init(sy.bar(B_O_FULL + t), 1);
-      ptx::mbar_init(sy.bar(B_O_EMPTY + t), BM);
       ptx::mbar_init(sy.bar(B_SCHED_FULL + t), 1);
-      ptx::mbar_init(sy.bar(B_SCHED_EMPTY + t), 9);  // MMA warp + 8 softmax warps
+      ptx::mbar_init(sy.bar(B_SCHED_EMPTY + t), 9);  // 8 softmax warps + the issuing thread
+      ptx::mbar_init(sy.bar(B_FINAL + t), 1);
+      ptx::mbar_init(sy.bar(B_P_DONE + t), 4);   // one arrival per warp of the sub-tile
+      ptx::mbar_init(sy.bar(B_O_READ + t), 4);
     }
-    ptx::mbar_init(sy.bar(B_FINAL), 1);
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(sy.bar(B_KV + s), 1);
       ptx::mbar_init(sy.bar(B_KV + C::kStages + s), 1);
@@ -198,7 +214,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kAllocWarp) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
@@ -207,9 +223,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------ scheduler + TMA producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    ptx::setmaxnreg_dec<kRegsControl>();
+    if (warp == kTmaWarp && lane == 0) {
+      // ---------------------------------------------- scheduler + TMA producer
       uint32_t q_uses[2] = {0, 0};
       uint32_t kv_it = 0;
       for (uint32_t it = 0;; ++it) {
@@ -273,135 +290,146 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
       }
     }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------------- MMA issue
-    constexpr uint32_t kIdescQK = ptx::idesc_f16(BF16, BM, BN, false);
-    constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, BM, D, true);
-    uint32_t q_uses[2] = {0, 0}, p_cnt[2] = {0, 0}, o_uses[2] = {0, 0};
-    uint32_t kv_it = 0;
-    bool issued_any = false;
-    // S_t = Q_t K^T over d: K = 16 per instruction, 4 steps per 128-byte swizzle atom
-    auto issue_qk = [&](int t, int kstage) {
-      const uint32_t qa = sbase + C::kOffQ + t * C::kTileBytes;
-      const uint32_t ka = sbase + C::kOffKV + kstage * C::kTileBytes;
+    if (warp == kIssueWarp && lane == 0) {
+      // ------------------------------------------------------------ MMA issue
+      // One thread issues for both sub-tiles, in the order
+      //   QK0(0), QK1(0) | PV0(0), QK0(1), PV1(0), QK1(1) | PV0(1), QK0(2), ...
+      // so the two sub-tiles' batches B_t(j) = {PV_t(j), QK_t(j+1)} alternate on
+      // the tensor core and each softmax runs while the other sub-tile's MMAs
+      // execute. Everything a batch needs except P (V_j, K_{j+1}) is waited for
+      // first, then P_t(j), then the batch is issued back to back. The commit that
+      // signals S_t(j+1) also covers PV_t(j), and P_t(j) (which overwrites S_t) is
+      // read before QK_t(j+1) rewrites S_t because both are issued by this thread
+      // in that order.
+      constexpr uint32_t kIdescQK = ptx::idesc_f16(BF16, BM, BN, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_f16(BF16, BM, D, true);
+      // descriptors of the operand bases; the start-address field (bits 0-13,
+      // address >> 4) of each instruction's operand is the base plus a small offset
+      // that stays inside the field, so a 64-bit add of (offset >> 4) selects it
+      const uint64_t dq0 = ptx::sdesc_sw128(sbase + C::kOffQ, 16, 1024);
+      const uint64_t dkv0 = ptx::sdesc_sw128(sbase + C::kOffKV, 16, 1024);
+      const uint64_t dv0 = ptx::sdesc_sw128(sbase + C::kOffKV, BN * 128, 1024);
+      auto issue_qk = [&](int t, int kstage) {
+        const uint64_t qa = dq0 + (uint64_t)((t * C::kTileBytes) >> 4);
+        const uint64_t ka = dkv0 + (uint64_t)((kstage * C::kTileBytes) >> 4);
+        const uint32_t dS = tmem + (uint32_t)(C::kColS + t * BN);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (uint32_t)((kk >> 2) * BN * 128 + (kk & 3) * 32);
-        ptx::mma_ss(tmem + C::kColS + t * BN, ptx::sdesc_sw128(qa + off, 16, 1024),
-                    ptx::sdesc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-      }
-    };
-    // O_t += P_t V over keys: K = 16 keys per instruction; P from TMEM (8 columns
-    // per 16 keys), V MN-major (d contiguous): 8-key groups 1024 B apart, 64-wide
-    // d atoms BN*128 B apart
-    auto issue_pv = [&](int t, int vstage, bool accumulate) {
-      const uint32_t va = sbase + C::kOffKV + vstage * C::kTileBytes;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
+          ptx::mma_ss(dS, qa + off, ka + off, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V over the first 16*nk keys: P from TMEM (8 columns per 16
+      // keys), V MN-major (d contiguous): 8-key groups 1024 B apart, 64-wide d atoms
+      // BN*128 B apart
+      auto issue_pv = [&](int t, int vstage, bool accumulate, int nk) {
+        const uint64_t va = dv0 + (uint64_t)((vstage * C::kTileBytes) >> 4);
+        const uint32_t dO = tmem + (uint32_t)(C::kColO + t * D);
+        const uint32_t aP = tmem + (uint32_t)(C::kColS + t * BN);
+        if (nk == BN / 16) {
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
-        ptx::mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * BN + kk * 8,
-                    ptx::sdesc_sw128(va + kk * 2048, BN * 128, 1024), kIdescPV,
-                    (accumulate || kk > 0) ? 1u : 0u);
-      }
-    };
-    for (uint32_t it = 0;; ++it) {
-      const int slot = (int)(it & 1u);
-      if (!sy.wait_warp(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
-      const UnitInfo u = info[slot];
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
-      if (u.w >= num_tiles) break;
-      const int n0 = u.n_kv[0], n1 = u.n_kv[1];
-      const int n_tiles = max(n0, n1);
-      if (n_tiles == 0) continue;
-      const int nt[2] = {n0, n1};
-      bool ok = true;
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (ok && nt[t] > 0) ok = sy.wait_warp(B_Q_FULL + t, (q_uses[t]++) & 1u);
-      if (!ok) break;
-      // prologue: S_t(0)
-      int kstage = (int)(kv_it % C::kStages);
-      if (!sy.wait_warp(B_KV + kstage, (kv_it / C::kStages) & 1u)) break;
-      ++kv_it;
-      ptx::tc_fence_after();
-      if (lane == 0) {
+          for (int kk = 0; kk < BN / 16; ++kk)
+            ptx::mma_ts(dO, aP + kk * 8, va + (uint64_t)(kk * 128), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        } else {
+          for (int kk = 0; kk < nk; ++kk)
+            ptx::mma_ts(dO, aP + kk * 8, va + (uint64_t)(kk * 128), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto kv_stage = [](uint32_t fill) { return (int)(fill % C::kStages); };
+      auto kv_phase = [](uint32_t fill) { return (fill / C::kStages) & 1u; };
+      uint32_t q_uses[2] = {0, 0}, p_waits[2] = {0, 0}, o_reads_seen[2] = {0, 0}, o_read_waits[2] = {0, 0};
+      uint32_t kv_base = 0;
+      bool issued_any = false, ok = true;
+      for (uint32_t it = 0; ok; ++it) {
+        const int slot = (int)(it & 1u);
+        if (!sy.wait(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
+        const UnitInfo u = info[slot];
+        ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
+        if (u.w >= num_tiles) break;
+        const int nt[2] = {u.n_kv[0], u.n_kv[1]};
+        const int n_tiles = max(nt[0], nt[1]);
+        if (n_tiles == 0) continue;
+        ok = sy.wait(B_KV + kv_stage(kv_base), kv_phase(kv_base));
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (nt[t] == 0) continue;
-          issue_qk(t, kstage);
+          if (!ok || nt[t] == 0) continue;
+          ok = sy.wait(B_Q_FULL + t, (q_uses[t]++) & 1u);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_qk(t, kv_stage(kv_base));
           ptx::tc_commit(sy.bar(B_S_FULL + t));
           if (nt[t] == 1) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
         }
-        ptx::tc_commit(sy.bar(B_KV + C::kStages + kstage));
+        if (!ok) break;
+        ptx::tc_commit(sy.bar(B_KV + C::kStages + kv_stage(kv_base)));
         issued_any = true;
-      }
-      __syncwarp();
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int vstage = (int)(kv_it % C::kStages);
-        if (!(ok = sy.wait_warp(B_KV + vstage, (kv_it / C::kStages) & 1u))) break;
-        ++kv_it;
-        if (j == n_tiles - 1 && (j + 1) * BN > u.len_k) {
-          // zero V rows [valid, BN) of the tail tile (whole 128-byte rows: swizzle-agnostic)
-          const int valid = u.len_k - j * BN;
-          const int chunks_per_half = (BN - valid) * 8;
-          uint8_t* vt = smem + C::kOffKV + vstage * C::kTileBytes;
-          for (int idx = lane; idx < chunks_per_half * C::kHalves; idx += 32) {
-            const int hf = idx / chunks_per_half;
-            const int within = idx - hf * chunks_per_half;
-            *reinterpret_cast<uint4*>(vt + hf * BN * 128 + valid * 128 + within * 16) = make_uint4(0, 0, 0, 0);
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-        }
-        int knext = -1;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const uint32_t vfill = kv_base + 2u * (uint32_t)j + 1u;
+          const uint32_t kfill = kv_base + 2u * (uint32_t)(j + 1);
+          const int vstage = kv_stage(vfill);
+          const int kstage = kv_stage(kfill);
+          const bool kmore = j + 1 < n_tiles;
+          ok = sy.wait(B_KV + vstage, kv_phase(vfill)) && (!kmore || sy.wait(B_KV + kstage, kv_phase(kfill)));
           if (!ok) break;
-          if (j < nt[t]) {
-            if (j == 0 && !(ok = sy.wait_warp(B_O_EMPTY + t, (o_uses[t]++ & 1u) ^ 1u))) break;
-            if (!(ok = sy.wait_warp(B_P_FULL + t, (p_cnt[t]++) & 1u))) break;
-            ptx::tc_fence_after();
-            if (lane == 0) {
-              issue_pv(t, vstage, j > 0);
-              if (j + 1 == nt[t]) ptx::tc_commit(sy.bar(B_O_FULL + t));
+          // keys of this tile that exist: PV runs over ceil(valid/16) steps of 16
+          // keys, and the at most 15 rows between valid and that bound are zeroed
+          // (pad rows may hold NaN and 0 * NaN = NaN); whole 128-byte rows, so
+          // swizzle-agnostic
+          int nk = BN / 16;
+          if ((j + 1) * BN > u.len_k) {
+            const int valid = u.len_k - j * BN;
+            nk = (valid + 15) >> 4;
+            const int zrows = nk * 16 - valid;
+            if (zrows > 0) {
+              uint8_t* vt = smem + C::kOffKV + vstage * C::kTileBytes;
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                for (int idx = 0; idx < zrows * 8; ++idx)
+                  *reinterpret_cast<uint4*>(vt + hf * BN * 128 + valid * 128 + idx * 16) = make_uint4(0, 0, 0, 0);
+              ptx::fence_proxy_async_smem();
             }
-            __syncwarp();
           }
-          if (t == 0 && j + 1 < n_tiles) {
-            knext = (int)(kv_it % C::kStages);
-            if (!(ok = sy.wait_warp(B_KV + knext, (kv_it / C::kStages) & 1u))) break;
-            ++kv_it;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || j >= nt[t]) continue;
+            // the previous unit's epilogue has read O_t before PV_t(0) overwrites it
+            while (ok && j == 0 && o_read_waits[t] < o_reads_seen[t])
+              ok = sy.wait(B_O_READ + t, (o_read_waits[t]++) & 1u);
+            ok = ok && sy.wait(B_P_DONE + t, (p_waits[t]++) & 1u);
+            if (!ok) break;
             ptx::tc_fence_after();
-          }
-          if (j + 1 < nt[t]) {
-            if (lane == 0) {
-              issue_qk(t, knext);
+            issue_pv(t, vstage, j > 0, nk);
+            if (j + 1 < nt[t]) {
+              issue_qk(t, kstage);
               ptx::tc_commit(sy.bar(B_S_FULL + t));
               if (j + 2 == nt[t]) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
+            } else {
+              ptx::tc_commit(sy.bar(B_O_FULL + t));
             }
-            __syncwarp();
           }
-        }
-        if (!ok) break;
-        if (lane == 0) {
-          if (knext >= 0) ptx::tc_commit(sy.bar(B_KV + C::kStages + knext));
+          if (!ok) break;
           ptx::tc_commit(sy.bar(B_KV + C::kStages + vstage));
+          if (kmore) ptx::tc_commit(sy.bar(B_KV + C::kStages + kstage));
         }
-        __syncwarp();
+        kv_base += 2u * (uint32_t)n_tiles;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (nt[t] > 0) ++o_reads_seen[t];
       }
-      if (!ok) break;
-    }
-    // drain every MMA this thread issued before TMEM is released
-    if (lane == 0 && issued_any) {
-      ptx::tc_commit(sy.bar(B_FINAL));
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(sy.bar(B_FINAL), 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+      // drain every MMA this thread issued before TMEM is released
+      if (issued_any) {
+        ptx::tc_commit(sy.bar(B_FINAL));
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(sy.bar(B_FINAL), 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
       }
     }
     __syncwarp();
   } else {
-    // -------------------------------------------------------------- softmax
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    // ---------------------------------------------------------- softmax, per sub-tile
+    // Warpgroup t owns query rows [row0 + 128 t, row0 + 128 t + 128) of the unit:
+    // its threads turn S_t into P_t in TMEM, rescale O_t when the running max
+    // moves, and write O_t and the LSE at the end of the unit.
     const int t = warp >> 2;                    // sub-tile
     const int row = ((warp & 3) << 5) + lane;   // TMEM lane == query row within the sub-tile
     const uint32_t lane_bits = (uint32_t)((warp & 3) << 5) << 16;
@@ -409,6 +437,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const uint32_t tO = tmem + lane_bits + (uint32_t)(C::kColO + t * D);
     const float sl2 = p.scale_log2;
     T* __restrict__ O = static_cast<T*>(p.o);
+    // warp-level arrival on a barrier the issuing thread waits on (bounded), after
+    // this thread's tcgen05 stores/loads are complete
+    auto warp_arrive = [&](int b) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sy.bar(b));
+    };
     uint32_t s_cnt = 0, o_cnt = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = (int)(it & 1u);
@@ -417,9 +452,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
       if (u.w >= num_tiles) break;
+      const int n = t ? u.n_kv[1] : u.n_kv[0];
       const int nrows = t ? u.n_rows[1] : u.n_rows[0];
       if (nrows == 0) continue;
-      const int n = t ? u.n_kv[1] : u.n_kv[0];
       const int r = u.row0 + t * BM + row;      // row inside the sequence
       const bool live = row < nrows;
       const int kmax_row = (int)max64(0, min64((int64_t)u.len_k, (int64_t)r + u.shift + 1));
@@ -434,22 +469,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld(s[c]);
         const int lim = kmax_row - j * BN;      // columns >= lim are not visible
-        float mx = -INFINITY;
-        if (lim >= BN) {
+        if (lim < BN) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float v = (c * 32 + i < lim) ? __uint_as_float(s[c][i]) : -INFINITY;
-              s[c][i] = __float_as_uint(v);
-              mx = fmaxf(mx, v);
-            }
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= lim) s[c][i] = __float_as_uint(-INFINITY);
         }
+        // row max: 8 independent chains of 3-input max
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaxf(__uint_as_float(s[0][q]), __uint_as_float(s[0][q + 8]));
+#pragma unroll
+        for (int i = 16; i < 128; i += 16)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            acc[q] = ptx::fmax3(acc[q], __uint_as_float(s[(i + q) >> 5][(i + q) & 31]),
+                                __uint_as_float(s[(i + q + 8) >> 5][(i + q + 8) & 31]));
+        const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
+                                    fmaxf(acc[6], acc[7]));
         // reference max in the log2 domain; moved only when the tile max exceeds it
         // by more than 8 (values of p stay below 2^8), so O is rescaled rarely
         const float mt = mx * sl2;
@@ -461,7 +499,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         l *= alpha;
         const float mref = (m == -INFINITY) ? 0.f : m;
-        float rs = 0.f;
+        const uint64_t scale2 = ptx::f2_pack(sl2, sl2);
+        const uint64_t shift2 = ptx::f2_pack(-mref, -mref);
+        uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int hp = 0; hp < 2; ++hp) {         // keys [64*hp, 64*hp+64) -> P columns [32*hp, 32*hp+32)
           uint32_t pk[32];
@@ -470,14 +510,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const int c = 2 * hp + c2;
-              const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][i]), sl2, -mref));
-              const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][i + 1]), sl2, -mref));
-              rs += p0 + p1;
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])),
+                                         scale2, shift2),
+                             x0, x1);
+              const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+              sum2[(i >> 1) & 3] = ptx::f2_add(sum2[(i >> 1) & 3], ptx::f2_pack(p0, p1));
               pk[c2 * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
             }
           ptx::tmem_st32(tS + 32 * hp, pk);
         }
-        l += rs;
+        {
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ptx::f2_add(sum2[0], sum2[1]), a0, a1);
+          ptx::f2_unpack(ptx::f2_add(sum2[2], sum2[3]), b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // O_t already holds PV of tiles < j (the commit of S_t(j) covered PV_t(j-1))
 #pragma unroll
@@ -491,8 +539,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
         }
         ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(sy.bar(B_P_FULL + t));
+        warp_arrive(B_P_DONE + t);               // this warp's rows of P_t(j) (and O_t rescale) stored
       }
       if (!ok) break;
       // epilogue: O = O_acc / l on live rows, LSE = (m + log2 l) * ln 2; dead rows 0 / -inf
@@ -517,8 +564,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
           }
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(sy.bar(B_O_EMPTY + t));
+        // every thread's reads of O_t complete before the issuing thread's next PV_t
+        warp_arrive(B_O_READ + t);
       } else if (live) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
@@ -534,7 +581,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, 512);
+  if (warp == kAllocWarp) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

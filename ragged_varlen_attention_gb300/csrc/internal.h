@@ -12,8 +12,16 @@ namespace thd {
 
 // Words of the workspace header. The tile counter is word 0 (the persistent
 // scheduler's claim counter); everything after it is sized by the plan.
-enum HeaderWord : int { kHdrCounter = 0, kHdrStatus = 1, kHdrNumPairs = 2, kHdrNumTiles = 3 };
-constexpr int kHeaderBytes = 64;
+// Words kHdrGroupStart .. kHdrGroupStart + kCostGroups hold the first pair index
+// of each cost group (cost = KV tiles a pair visits; group 0 = costs 512..1023,
+// group 1 = 256..511, ..., group 9 = cost 1, group 10 = cost 0), the last word
+// being the pair count.
+enum HeaderWord : int {
+  kHdrCounter = 0, kHdrStatus = 1, kHdrNumPairs = 2, kHdrNumTiles = 3, kHdrGroupStart = 4
+};
+constexpr int kCostGroups = 11;
+constexpr int kHeaderBytes = 128;
+static_assert((kHdrGroupStart + kCostGroups + 1) * 4 <= kHeaderBytes, "header words");
 
 // Per-sequence record written by the setup kernel. `shift` is the causal shift:
 // query row i sees keys j < len_k with j <= i + shift (mask 0 stores len_k, which
@@ -72,6 +80,25 @@ struct FwdParams {
   const SeqMeta* meta;
   const PairRec* pairs;
 };
+
+// Work id -> (pair index into the pair list, query head). Pairs are sorted by
+// descending cost; inside one cost group the order is kv head, then pair, then
+// query head of the kv group, so units that read the same K/V (same sequence and
+// kv head) run close together in time and share it through L2.
+__device__ __forceinline__ void work_to_unit(const uint32_t* header, uint32_t w, int h_q, int h_kv, int& pair,
+                                             int& head) {
+  const uint32_t grp = (uint32_t)(h_q / h_kv);
+  int g = 0;
+  while (g < kCostGroups - 1 && w >= header[kHdrGroupStart + g + 1] * (uint32_t)h_q) ++g;
+  const uint32_t start = header[kHdrGroupStart + g];
+  const uint32_t size = header[kHdrGroupStart + g + 1] - start;
+  const uint32_t local = w - start * (uint32_t)h_q;
+  const uint32_t per_kvh = size * grp;
+  const uint32_t kvh = local / per_kvh;
+  const uint32_t rem = local - kvh * per_kvh;
+  pair = (int)(start + rem / grp);
+  head = (int)(kvh * grp + rem % grp);
+}
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }

@@ -53,6 +53,9 @@ __device__ __forceinline__ int32_t pair_cost(const SeqMeta& m, int32_t row0, int
   return (int32_t)((kmax + keys_per_tile - 1) / keys_per_tile);
 }
 
+// group of a (clamped) cost: 0 for 512..1023, 1 for 256..511, ..., 9 for 1, 10 for 0
+__device__ __forceinline__ int cost_group(int32_t c) { return c == 0 ? kCostGroups - 1 : 9 - (31 - __clz(c)); }
+
 __device__ __forceinline__ int32_t find_seq(const int32_t* pair_base, int32_t batch, int32_t e) {
   // last b with pair_base[b] <= e (pair_base is non-decreasing, pair_base[0] == 0)
   int32_t lo = 0, hi = batch;  // answer in [lo, hi)
@@ -65,11 +68,13 @@ __device__ __forceinline__ int32_t find_seq(const int32_t* pair_base, int32_t ba
 
 __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   __shared__ uint32_t hist[kCostBins];
+  __shared__ uint32_t group_count[kCostGroups];
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   __shared__ uint32_t status_s;
   const int tid = threadIdx.x;
   for (int i = tid; i < kCostBins; i += blockDim.x) hist[i] = 0;
+  if (tid < kCostGroups) group_count[tid] = 0;
   if (tid == 0) { carry = 0; status_s = 0; }
   __syncthreads();
 
@@ -133,6 +138,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
     const int32_t c = min(pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile), kCostBins - 1);
     atomicAdd(&hist[c], 1u);
+    atomicAdd(&group_count[cost_group(c)], 1u);
   }
   __syncthreads();
 
@@ -158,6 +164,12 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   }
   __syncthreads();
   if (tid == 0) {
+    uint32_t acc = 0;
+    for (int g = 0; g < kCostGroups; ++g) {
+      p.header[kHdrGroupStart + g] = acc;
+      acc += group_count[g];
+    }
+    p.header[kHdrGroupStart + kCostGroups] = acc;
     p.header[kHdrCounter] = 0u;
     p.header[kHdrStatus] = status_s;
     p.header[kHdrNumPairs] = (uint32_t)total;

@@ -13,6 +13,40 @@ from __future__ import annotations
 import numpy as np
 
 COST_BINS = 1024
+COST_GROUPS = 11
+
+
+def cost_group(c: int) -> int:
+    """0 for costs 512..1023, 1 for 256..511, ..., 9 for 1, 10 for 0."""
+    return COST_GROUPS - 1 if c == 0 else 9 - (int(c).bit_length() - 1)
+
+
+def group_starts(pairs) -> list[int]:
+    """First pair index of each cost group in the longest-first list, plus the count."""
+    counts = [0] * COST_GROUPS
+    for _, _, c in pairs:
+        counts[cost_group(c)] += 1
+    out, acc = [], 0
+    for n in counts:
+        out.append(acc)
+        acc += n
+    return out + [acc]
+
+
+def unit_order(starts, h_q: int, h_kv: int):
+    """(pair index, query head) of every work id: inside a cost group kv head, then
+    pair, then query head of the kv group."""
+    grp = h_q // h_kv
+    out = []
+    for g in range(COST_GROUPS):
+        a, b = starts[g], starts[g + 1]
+        for kvh in range(h_kv):
+            for pr in range(a, b):
+                for hh in range(grp):
+                    out.append((pr, kvh * grp + hh))
+    return out
+
+
 BAD_LENGTH, BAD_OFFSET, BAD_MASK, TILE_OVERFLOW = 1, 2, 4, 8
 
 

@@ -147,3 +147,18 @@ def test_status_strings(lib):
 def test_package_import_does_not_load_library():
     # importing the package is side-effect free; the binding loads the library lazily
     assert hasattr(rva, "thd_attn_forward")
+
+
+def test_unit_order_covers_every_pair_and_head_once():
+    """The work-id -> (pair, head) order of the schedule is a permutation that keeps
+    the longest-first cost groups and puts query heads of one kv head innermost."""
+    from tests import schedule_mirror as sm
+    pairs = [(0, 0, 600), (1, 0, 300), (1, 256, 290), (2, 0, 3), (3, 0, 0)]
+    starts = sm.group_starts(pairs)
+    assert starts[0] == 0 and starts[-1] == len(pairs)
+    order = sm.unit_order(starts, h_q=8, h_kv=2)
+    assert sorted(order) == sorted((p, h) for p in range(len(pairs)) for h in range(8))
+    # group of pair 0 (cost 600) first; inside group 1 (costs 256..511): kv head 0's
+    # units (query heads 0-3) for pairs 1 and 2 before kv head 1's
+    assert order[:8] == [(0, h) for h in range(4)] + [(0, h) for h in range(4, 8)]
+    assert order[8:16] == [(1, 0), (1, 1), (1, 2), (1, 3), (2, 0), (2, 1), (2, 2), (2, 3)]

@@ -113,10 +113,12 @@ def test_schedule_matches_cpu_mirror(kernel):
     plan = res["plan"]
     ws = res["ws"].cpu().numpy()
     hdr, meta_off, base_off, pairs_off = plan.workspace_layout
-    header = ws[hdr:hdr + 16].view(np.uint32)
+    header = ws[hdr:hdr + 128].view(np.uint32)
     meta_exp, pairs_exp, status_exp, n_exp = schedule_mirror.mirror(
         batch, plan.rows_per_unit, plan.keys_per_tile, plan.max_pairs)
     assert header[1] == status_exp and header[2] == n_exp and header[3] == n_exp * batch.h_q
+    starts = schedule_mirror.group_starts(pairs_exp)
+    assert list(header[4:4 + len(starts)]) == starts
     meta = ws[meta_off:meta_off + 32 * batch.batch].view(np.int32).reshape(batch.batch, 8)
     assert np.array_equal(meta, meta_exp)
     pairs = ws[pairs_off:pairs_off + 8 * n_exp].view(np.int32).reshape(n_exp, 2)
