@@ -107,7 +107,17 @@ typedef struct {
   thd_stats_layout_t stats_layout;
   float softmax_scale;            /* NaN => 1/sqrt(d) */
   thd_kernel_t kernel;
+  uint32_t flags;                 /* THD_FLAG_* bits */
 } thd_attn_desc_t;
+
+/* Plan flags.
+ * THD_FLAG_NO_KV_SPLIT: never split a unit's key range. By default, when a launch
+ *   has fewer than about four waves of work units for the GPU, the tensor-core
+ *   path processes long units as two halves of their key range and merges the
+ *   halves' partial results (log-sum-exp weighted) in a small follow-up kernel,
+ *   which evens out the last wave. The partial results live in the workspace, so
+ *   splitting enlarges workspace_bytes; this flag keeps the workspace small. */
+enum { THD_FLAG_NO_KV_SPLIT = 1u << 0 };
 
 typedef struct thd_attn_plan_s* thd_attn_plan_t;
 
@@ -151,11 +161,12 @@ thd_kernel_t thd_attn_plan_kernel(thd_attn_plan_t plan);
 void thd_attn_plan_geometry(thd_attn_plan_t plan, int32_t* rows_per_unit,
                             int32_t* keys_per_tile, int32_t* max_pairs);
 
-/* Byte offsets, inside the workspace, of its four regions: [0] header words
- * (tile counter, status, pair count, tile count), [1] per-sequence metadata
- * (8 int32 per sequence: len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift),
- * [2] per-sequence first pair index (int32 [B+1]), [3] the scheduled pair list
- * (int32 {b, first query row} per pair, longest first). For inspection only. */
+/* Byte offsets, inside the workspace, of its first four regions: [0] header words
+ * (tile counter, status, entry count, tile count, first entry of each cost group,
+ * split count), [1] per-sequence metadata (8 int32 per sequence: len_q, len_k,
+ * off_q, off_k, off_v, off_o, off_s, shift), [2] per-sequence first pair index
+ * (int32 [B+1]), [3] the scheduled entry list (int32 {b, first query row, split,
+ * partial slot} per entry, longest first). For inspection only. */
 void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]);
 
 void thd_attn_plan_destroy(thd_attn_plan_t plan);
@@ -188,7 +199,8 @@ int64_t thd_attn_view_span_bytes(int64_t rows, int64_t heads, int64_t d, int64_t
  * static device array of thd_attn_static_workspace_capacity() bytes (1 MiB) that
  * each GPU loading this library keeps until the process exits. The call makes no
  * allocation of any kind. Returns THD_ERR_WORKSPACE when the plan's
- * workspace_bytes exceed that capacity.
+ * workspace_bytes exceed that capacity (plan with THD_FLAG_NO_KV_SPLIT: the
+ * partial results of split key ranges do not fit the static array).
  *
  * The first call on each device (with that device current) looks up the array's
  * device address with cudaGetSymbolAddress; make it before any stream capture.

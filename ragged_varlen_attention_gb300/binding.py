@@ -14,6 +14,7 @@ import torch
 
 STATS_TOKEN_MAJOR, STATS_HEAD_MAJOR = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05 = 0, 1, 2
+FLAG_NO_KV_SPLIT = 1
 _DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 _STATUS = {0: "THD_OK", 1: "THD_ERR_INVALID_ARG", 2: "THD_ERR_UNSUPPORTED",
            3: "THD_ERR_ALIGNMENT", 4: "THD_ERR_CAPACITY", 5: "THD_ERR_WORKSPACE",
@@ -44,6 +45,7 @@ class ThdAttnDesc(ctypes.Structure):
         ("stats_layout", ctypes.c_int),
         ("softmax_scale", ctypes.c_float),
         ("kernel", ctypes.c_int),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -128,7 +130,7 @@ def _view_bytes(t: torch.Tensor) -> int:
 def make_desc(dtype: torch.dtype, batch: int, h_q: int, h_kv: int, d: int, cap_rows, stride_tok,
               stride_head, nbytes=(0, 0, 0, 0), cap_rows_stats: int = 0,
               stats_layout: int = STATS_TOKEN_MAJOR, softmax_scale: float | None = None,
-              kernel: int = KERNEL_AUTO) -> ThdAttnDesc:
+              kernel: int = KERNEL_AUTO, flags: int = 0) -> ThdAttnDesc:
     desc = ThdAttnDesc()
     desc.dtype = _DTYPE_CODE[dtype]
     desc.batch, desc.h_q, desc.h_kv, desc.d = batch, h_q, h_kv, d
@@ -141,6 +143,7 @@ def make_desc(dtype: torch.dtype, batch: int, h_q: int, h_kv: int, d: int, cap_r
     desc.stats_layout = int(stats_layout)
     desc.softmax_scale = math.nan if softmax_scale is None else float(softmax_scale)
     desc.kernel = int(kernel)
+    desc.flags = int(flags)
     return desc
 
 
@@ -155,7 +158,7 @@ def thd_attn_plan(desc: ThdAttnDesc) -> ThdAttnPlan:
 
 
 def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: int,
-                     softmax_scale=None, kernel: int = KERNEL_AUTO) -> ThdAttnPlan:
+                     softmax_scale=None, kernel: int = KERNEL_AUTO, flags: int = 0) -> ThdAttnPlan:
     """Build a plan from [rows, heads, d] tensor views (last dim contiguous)."""
     for t in (q, k, v, o):
         if t.dim() != 3 or t.stride(2) != 1:
@@ -163,7 +166,7 @@ def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: 
     desc = make_desc(q.dtype, batch, q.shape[1], k.shape[1], q.shape[2],
                      [t.shape[0] for t in (q, k, v, o)], [t.stride(0) for t in (q, k, v, o)],
                      [t.stride(1) for t in (q, k, v, o)], [_view_bytes(t) for t in (q, k, v, o)],
-                     cap_rows_stats, stats_layout, softmax_scale, kernel)
+                     cap_rows_stats, stats_layout, softmax_scale, kernel, flags)
     return thd_attn_plan(desc)
 
 

@@ -132,16 +132,27 @@ thd_status_t thd_attn_plan(thd_attn_plan_t* out, const thd_attn_desc_t* desc, si
   }
   // non-overlapping O rows bound the number of (sequence, query tile) pairs
   const int64_t max_pairs = (int64_t)d.batch + (d.cap_rows[3] + p->rows_per_unit - 1) / p->rows_per_unit + 1;
-  if (max_pairs * d.h_q >= (int64_t(1) << 31)) {
+  if (2 * max_pairs * d.h_q >= (int64_t(1) << 31)) {
     delete p;
     return THD_ERR_UNSUPPORTED;
   }
   p->max_pairs = (int32_t)max_pairs;
+  // KV split (tensor-core path): it only triggers below kSplitWaves waves of units,
+  // i.e. for fewer than kSplitWaves * SMs / h_q pairs, which bounds the split table
+  // and the partial-result buffers
+  p->allow_split = kernel == THD_KERNEL_TCGEN05 && !(d.flags & THD_FLAG_NO_KV_SPLIT);
+  const int64_t split_bound = ((int64_t)thd::kSplitWaves * thd::kMaxSmsForSizing + d.h_q - 1) / d.h_q;
+  p->max_split = p->allow_split ? (int32_t)(max_pairs < split_bound ? max_pairs : split_bound) : 0;
+  const int64_t part_rows = (int64_t)p->max_split * 2 * d.h_q * p->rows_per_unit;
   int64_t off = 0;
   p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
   p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
   p->ws_off[2] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
-  p->ws_off[3] = off; off = align_up(off + max_pairs * (int64_t)sizeof(thd::PairRec), kAlign);
+  p->ws_off[3] = off;
+  off = align_up(off + (p->allow_split ? 2 : 1) * max_pairs * (int64_t)sizeof(thd::PairRec), kAlign);
+  p->ws_off[4] = off; off = align_up(off + (int64_t)p->max_split * (int64_t)sizeof(thd::SplitRec), kAlign);
+  p->ws_off[5] = off; off = align_up(off + part_rows * d.d * 4, kAlign);
+  p->ws_off[6] = off; off = align_up(off + part_rows * 4, kAlign);
   p->ws_bytes = (size_t)off;
   *ws_bytes = p->ws_bytes;
   *out = p;
@@ -158,6 +169,7 @@ void thd_attn_plan_geometry(thd_attn_plan_t plan, int32_t* rows, int32_t* keys, 
 }
 
 void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]) {
+  // the first four regions; the split table and partial buffers follow
   if (!plan || !offsets) return;
   for (int i = 0; i < 4; ++i) offsets[i] = plan->ws_off[i];
 }
@@ -247,10 +259,13 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   sp.keys_per_tile = plan->keys_per_tile;
   sp.max_pairs = plan->max_pairs;
   sp.h_q = d.h_q;
+  sp.allow_split = plan->allow_split;
+  sp.max_split = plan->max_split;
   sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
   sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
   sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
   sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
+  sp.splits = reinterpret_cast<thd::SplitRec*>(ws + plan->ws_off[4]);
 
   thd::FwdParams fp;
   fp.q = q; fp.k = k; fp.v = v; fp.o = o; fp.stats = stats;
@@ -267,6 +282,10 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   fp.status = sp.header + thd::kHdrStatus;
   fp.meta = sp.meta;
   fp.pairs = sp.pairs;
+  fp.splits = sp.splits;
+  fp.part_o = reinterpret_cast<float*>(ws + plan->ws_off[5]);
+  fp.part_lse = reinterpret_cast<float*>(ws + plan->ws_off[6]);
+  fp.rows_per_unit = plan->rows_per_unit;
 
   // a view with no rows has no TMA descriptor: the SIMT kernel serves that call
   // (it walks any unit size, so the plan's schedule geometry still applies)
@@ -281,6 +300,9 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
 
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return THD_ERR_CUDA;
+  // the tensor-core kernel's persistent grid: one CTA per SM
+  sp.num_ctas = use_tc ? thd::tc_grid_size(num_sms, plan->max_pairs, d.h_q) : num_sms;
+  if (!use_tc) sp.allow_split = 0;
   if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
   const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
   if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
@@ -289,6 +311,7 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   if (use_tc) {
     err = thd::launch_fwd_tc(fp, d, plan->max_pairs, num_sms, stream);
     if (err == cudaErrorNotSupported) return THD_ERR_UNSUPPORTED;
+    if (err == cudaSuccess && plan->allow_split) err = thd::launch_combine(fp, d.dtype, num_sms, stream);
   } else {
     err = thd::launch_fwd_simt(fp, d.dtype, plan->rows_per_unit, num_sms, stream);
   }

@@ -80,7 +80,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   static constexpr int kNumBars = B_KV + 2 * kStages;
   static constexpr int kOffInfo = kOffBar + kNumBars * 8;
-  static constexpr int kOffMisc = kOffInfo + 2 * 64;
+  static constexpr int kOffMisc = kOffInfo + 2 * 80;   // two UnitInfo slots
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kColS = 0;
   static constexpr int kColO = 256;
@@ -91,10 +91,13 @@ struct UnitInfo {
   uint32_t w;            // work id; >= num_tiles: no more work
   int32_t b, row0, h, g;
   int32_t len_k, off_q, off_k, off_v, off_o, off_s, shift;
-  int32_t n_kv[2];       // KV tiles each sub-tile visits
+  int32_t n_kv[2];       // KV tiles each sub-tile visits in this entry
   int32_t n_rows[2];     // valid query rows of each sub-tile
+  int32_t kv_lo;         // first KV tile of this entry (0 unless the second half of a split)
+  int32_t part_slot;     // partial-result slot (2 * part + half), -1 for a whole pair
+  int32_t pad[2];
 };
-static_assert(sizeof(UnitInfo) == 64, "UnitInfo is 64 bytes");
+static_assert(sizeof(UnitInfo) == 80, "UnitInfo is 80 bytes");
 
 struct Sync {
   uint32_t bar0;               // shared address of barrier 0
@@ -145,6 +148,9 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
   u.b = u.row0 = u.h = u.g = 0;
   u.len_k = u.off_q = u.off_k = u.off_v = u.off_o = u.off_s = u.shift = 0;
   u.n_kv[0] = u.n_kv[1] = u.n_rows[0] = u.n_rows[1] = 0;
+  u.kv_lo = 0;
+  u.part_slot = -1;
+  u.pad[0] = u.pad[1] = 0;
   if (w >= num_tiles) return u;
   int pair_idx, head;
   work_to_unit(p.header, w, p.h_q, p.h_kv, pair_idx, head);
@@ -157,6 +163,7 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
   u.len_k = m.len_k;
   u.off_q = m.off_q; u.off_k = m.off_k; u.off_v = m.off_v; u.off_o = m.off_o; u.off_s = m.off_s;
   u.shift = m.shift;
+  int full[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r_begin = pr.row0 + t * BM;
@@ -167,8 +174,20 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
       const int64_t kmax = min64((int64_t)m.len_k, (int64_t)(r_begin + rows - 1) + m.shift + 1);
       n = kmax > 0 ? (int)((kmax + BN - 1) / BN) : 0;
     }
-    u.n_kv[t] = n;
+    full[t] = n;
   }
+  // a split pair covers KV tiles [0, n/2) in its first half and [n/2, n) in its second
+  const int n_pair = max(full[0], full[1]);
+  const int halves = pr.split & 0xff, half = pr.split >> 8;
+  int lo = 0, hi = n_pair;
+  if (halves == 2) {
+    lo = half == 0 ? 0 : n_pair / 2;
+    hi = half == 0 ? n_pair / 2 : n_pair;
+    u.part_slot = 2 * pr.part + half;
+  }
+  u.kv_lo = lo;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) u.n_kv[t] = max(0, min(hi, full[t]) - lo);
   return u;
 }
 
@@ -260,7 +279,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             const uint32_t fbar = sy.bar(B_KV + stage);
             ptx::mbar_arrive_expect_tx(fbar, C::kTileBytes);
             const void* map = kv == 0 ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
-            const int row = (kv == 0 ? u.off_k : u.off_v) + j * BN;
+            const int row = (kv == 0 ? u.off_k : u.off_v) + (u.kv_lo + j) * BN;
 #pragma unroll
             for (int hf = 0; hf < C::kHalves; ++hf)
               ptx::tma_load_3d(sbase + C::kOffKV + stage * C::kTileBytes + hf * BN * 128, map, fbar, hf * 64, u.g,
@@ -376,8 +395,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           // (pad rows may hold NaN and 0 * NaN = NaN); whole 128-byte rows, so
           // swizzle-agnostic
           int nk = BN / 16;
-          if ((j + 1) * BN > u.len_k) {
-            const int valid = u.len_k - j * BN;
+          const int jj = u.kv_lo + j;            // absolute KV tile
+          if ((jj + 1) * BN > u.len_k) {
+            const int valid = u.len_k - jj * BN;
             nk = (valid + 15) >> 4;
             const int zrows = nk * 16 - valid;
             if (zrows > 0) {
@@ -468,7 +488,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld(s[c]);
-        const int lim = kmax_row - j * BN;      // columns >= lim are not visible
+        const int lim = kmax_row - (u.kv_lo + j) * BN;   // columns >= lim are not visible
         if (lim < BN) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -542,8 +562,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         warp_arrive(B_P_DONE + t);               // this warp's rows of P_t(j) (and O_t rescale) stored
       }
       if (!ok) break;
-      // epilogue: O = O_acc / l on live rows, LSE = (m + log2 l) * ln 2; dead rows 0 / -inf
+      // epilogue: O = O_acc / l on live rows, LSE = (m + log2 l) * ln 2; dead rows 0 / -inf.
+      // For half of a split pair the normalised partial O (fp32) and its base-2 LSE
+      // go to the partial buffers instead; the combine kernel merges the halves.
+      const bool partial = u.part_slot >= 0;
+      const int urow = t * BM + row;            // row within the unit
       T* orow = O + (int64_t)(u.off_o + r) * p.stride_tok[3] + (int64_t)u.h * p.stride_head[3];
+      float* prow = p.part_o + (((int64_t)u.part_slot * p.h_q + u.h) * p.rows_per_unit + urow) * D;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (n > 0) {
         if (!sy.wait_warp(B_O_FULL + t, (o_cnt++) & 1u)) break;
@@ -553,7 +578,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           uint32_t o[32];
           ptx::tmem_ld32(tO + 32 * c, o);
           ptx::tmem_wait_ld(o);
-          if (live) {
+          if (live && partial) {
+            float4* dst = reinterpret_cast<float4*>(prow + 32 * c);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
+                                    __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+          } else if (live) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -566,12 +597,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         // every thread's reads of O_t complete before the issuing thread's next PV_t
         warp_arrive(B_O_READ + t);
+      } else if (live && partial) {
+        float4* dst = reinterpret_cast<float4*>(prow);
+#pragma unroll
+        for (int q4 = 0; q4 < D / 4; ++q4) dst[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
       } else if (live) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
         for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
       }
-      if (live) {
+      if (live && partial) {
+        p.part_lse[((int64_t)u.part_slot * p.h_q + u.h) * p.rows_per_unit + urow] =
+            l > 0.f ? m + ptx::lg2(l) : -INFINITY;
+      } else if (live) {
         const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994530942f : -INFINITY;
         p.stats[(int64_t)(u.off_s + r) * p.stats_tok + (int64_t)u.h * p.stats_head] = lse;
       }
@@ -629,8 +667,7 @@ cudaError_t launch_impl(const FwdParams& p, const thd_attn_desc_t& desc, int max
   const int smem = C::kSmemBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int64_t max_tiles = (int64_t)max_pairs * desc.h_q;
-  const int grid = (int)max64(1, min64((int64_t)num_sms, max_tiles));
+  const int grid = tc_grid_size(num_sms, max_pairs, desc.h_q);
   fwd_tc_kernel<D, BF16><<<grid, kThreadsTC, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -638,6 +675,10 @@ cudaError_t launch_impl(const FwdParams& p, const thd_attn_desc_t& desc, int max
 }  // namespace
 
 bool tc_kernel_available() { return true; }
+int tc_grid_size(int num_sms, int max_pairs, int h_q) {
+  // entries: at most two per pair (KV split)
+  return (int)max64(1, min64((int64_t)num_sms, 2 * (int64_t)max_pairs * h_q));
+}
 int tc_rows_per_unit() { return 2 * BM; }
 int tc_keys_per_tile() { return BN; }
 

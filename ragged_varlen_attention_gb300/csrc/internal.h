@@ -17,11 +17,21 @@ namespace thd {
 // group 1 = 256..511, ..., group 9 = cost 1, group 10 = cost 0), the last word
 // being the pair count.
 enum HeaderWord : int {
-  kHdrCounter = 0, kHdrStatus = 1, kHdrNumPairs = 2, kHdrNumTiles = 3, kHdrGroupStart = 4
+  kHdrCounter = 0, kHdrStatus = 1, kHdrNumPairs = 2, kHdrNumTiles = 3, kHdrGroupStart = 4,
+  kHdrNumSplit = 16  // pairs whose KV range is split in two (partials merged by the combine kernel)
 };
 constexpr int kCostGroups = 11;
 constexpr int kHeaderBytes = 128;
-static_assert((kHdrGroupStart + kCostGroups + 1) * 4 <= kHeaderBytes, "header words");
+static_assert(kHdrGroupStart + kCostGroups + 1 <= kHdrNumSplit, "header words");
+static_assert((kHdrNumSplit + 1) * 4 <= kHeaderBytes, "header words");
+
+// KV split: when a launch has fewer than kSplitWaves waves of units, every pair
+// visiting at least kMinSplitCost KV tiles is processed as two halves of its KV
+// range whose partial results are merged afterwards. kMaxSmsForSizing bounds the
+// SM count the workspace is sized for.
+constexpr int kSplitWaves = 4;
+constexpr int kMinSplitCost = 4;
+constexpr int kMaxSmsForSizing = 160;
 
 // Per-sequence record written by the setup kernel. `shift` is the causal shift:
 // query row i sees keys j < len_k with j <= i + shift (mask 0 stores len_k, which
@@ -32,8 +42,16 @@ struct SeqMeta {
 static_assert(sizeof(SeqMeta) == 32, "SeqMeta is 32 bytes");
 
 // A scheduled unit: rows [row0, row0 + rows_per_unit) of sequence b, for every
-// query head (work id w -> pair w / h_q, head w % h_q).
+// query head. `split` = (half << 8) | halves: halves is 1 for a whole pair, 2 when
+// the pair's KV range [0, n) is processed as [0, n/2) and [n/2, n); `part` is
+// the pair's slot in the partial-result buffers (-1 when whole).
 struct PairRec {
+  int32_t b, row0, split, part;
+};
+static_assert(sizeof(PairRec) == 16, "PairRec is 16 bytes");
+
+// A pair whose KV range was split: where its rows are, for the combine kernel.
+struct SplitRec {
   int32_t b, row0;
 };
 
@@ -54,12 +72,16 @@ struct SetupParams {
   int32_t batch;
   int32_t rows_per_unit;
   int32_t keys_per_tile;
-  int32_t max_pairs;
+  int32_t max_pairs;        // pairs before splitting
   int32_t h_q;
+  int32_t allow_split;      // KV split permitted (workspace holds the partial buffers)
+  int32_t num_ctas;         // persistent CTAs of the attention kernel
+  int32_t max_split;        // capacity of the split-pair table
   uint32_t* header;
   SeqMeta* meta;
   int32_t* pair_base;       // [batch + 1]
-  PairRec* pairs;           // [max_pairs]
+  PairRec* pairs;           // [2 * max_pairs when splitting is allowed, else max_pairs]
+  SplitRec* splits;         // [max_split]
 };
 
 // Arguments common to both attention kernels.
@@ -79,6 +101,10 @@ struct FwdParams {
   uint32_t* status;
   const SeqMeta* meta;
   const PairRec* pairs;
+  const SplitRec* splits;
+  float* part_o;            // [max_split][2][h_q][rows_per_unit][d] normalised partial O
+  float* part_lse;          // [max_split][2][h_q][rows_per_unit] partial LSE, base 2
+  int32_t rows_per_unit;
 };
 
 // Work id -> (pair index into the pair list, query head). Pairs are sorted by
@@ -108,6 +134,7 @@ cudaError_t launch_setup(const SetupParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_simt(const FwdParams& p, thd_dtype_t dtype, int rows_per_unit, int num_sms,
                             cudaStream_t stream);
 int simt_rows_per_unit(int d);
+cudaError_t launch_combine(const FwdParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
 constexpr int kSimtKeysPerTile = 32;
 
 }  // namespace thd
@@ -122,7 +149,9 @@ struct thd_attn_plan_s {
   int64_t stats_tok, stats_head;
   int elem_bytes;
   size_t ws_bytes;
-  int64_t ws_off[4];        // header, meta, pair_base, pairs
+  int64_t ws_off[7];        // header, meta, pair_base, pairs, splits, part_o, part_lse
+  int32_t allow_split;
+  int32_t max_split;
   // optional attention-kernel timing (thd_attn_profile_enable)
   int32_t prof_slots;
   int32_t prof_count;

@@ -11,6 +11,10 @@
 //   2. histogram of tile costs (KV tiles to visit) in kCostBins buckets;
 //   3. descending exclusive scan of the histogram (longest tiles first);
 //   4. scatter of every (sequence, first row) pair to its bucket's next slot.
+// When a launch has fewer than kSplitWaves waves of units and splitting is
+// allowed, long pairs are scheduled as two halves of their KV range (two entries,
+// one partial-result slot, one record for the combine kernel), which evens out
+// the last wave of the persistent grid.
 // It also zeroes the persistent scheduler's tile counter (header word 0) and
 // writes the status word, pair count and tile count. Invalid sequences get no
 // tiles and set a status bit; their rows are never touched.
@@ -69,13 +73,15 @@ __device__ __forceinline__ int32_t find_seq(const int32_t* pair_base, int32_t ba
 __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   __shared__ uint32_t hist[kCostBins];
   __shared__ uint32_t group_count[kCostGroups];
+  __shared__ uint32_t n_splittable, n_split_done;
+  __shared__ bool split_on;
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   __shared__ uint32_t status_s;
   const int tid = threadIdx.x;
   for (int i = tid; i < kCostBins; i += blockDim.x) hist[i] = 0;
   if (tid < kCostGroups) group_count[tid] = 0;
-  if (tid == 0) { carry = 0; status_s = 0; }
+  if (tid == 0) { carry = 0; status_s = 0; n_splittable = 0; }
   __syncthreads();
 
   // 1. per-sequence metadata and tile counts
@@ -131,14 +137,38 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   }
   __syncthreads();
 
-  // 2. cost histogram
+  // 2a. KV split decision: with fewer than kSplitWaves waves of units, pairs that
+  // visit at least kMinSplitCost KV tiles are processed as two halves
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
-    const SeqMeta m = p.meta[b];
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    const int32_t c = min(pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile), kCostBins - 1);
-    atomicAdd(&hist[c], 1u);
-    atomicAdd(&group_count[cost_group(c)], 1u);
+    if (pair_cost(p.meta[b], row0, p.rows_per_unit, p.keys_per_tile) >= kMinSplitCost) atomicAdd(&n_splittable, 1u);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    split_on = p.allow_split && total > 0 &&
+               (int64_t)total * p.h_q < (int64_t)kSplitWaves * p.num_ctas && n_splittable > 0 &&
+               (int32_t)n_splittable <= p.max_split;
+    n_split_done = 0;
+  }
+  __syncthreads();
+
+  // 2b. cost histogram over the scheduled entries (a split pair gives two)
+  for (int32_t e = tid; e < total; e += blockDim.x) {
+    const int32_t b = find_seq(p.pair_base, p.batch, e);
+    const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
+    const int32_t cost = pair_cost(p.meta[b], row0, p.rows_per_unit, p.keys_per_tile);
+    if (split_on && cost >= kMinSplitCost) {
+      const int32_t c0 = min(cost / 2, kCostBins - 1), c1 = min(cost - cost / 2, kCostBins - 1);
+      atomicAdd(&hist[c0], 1u);
+      atomicAdd(&hist[c1], 1u);
+      atomicAdd(&group_count[cost_group(c0)], 1u);
+      atomicAdd(&group_count[cost_group(c1)], 1u);
+    } else {
+      const int32_t c = min(cost, kCostBins - 1);
+      atomicAdd(&hist[c], 1u);
+      atomicAdd(&group_count[cost_group(c)], 1u);
+    }
   }
   __syncthreads();
 
@@ -154,13 +184,27 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   // 4. scatter
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
-    const SeqMeta m = p.meta[b];
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    const int32_t c = min(pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile), kCostBins - 1);
-    const uint32_t slot = atomicAdd(&hist[c], 1u);
-    PairRec r;
-    r.b = b; r.row0 = row0;
-    p.pairs[slot] = r;
+    const int32_t cost = pair_cost(p.meta[b], row0, p.rows_per_unit, p.keys_per_tile);
+    if (split_on && cost >= kMinSplitCost) {
+      const int32_t part = (int32_t)atomicAdd(&n_split_done, 1u);
+      SplitRec sr;
+      sr.b = b; sr.row0 = row0;
+      p.splits[part] = sr;
+      for (int half = 0; half < 2; ++half) {
+        const int32_t c = min(half == 0 ? cost / 2 : cost - cost / 2, kCostBins - 1);
+        const uint32_t slot = atomicAdd(&hist[c], 1u);
+        PairRec r;
+        r.b = b; r.row0 = row0; r.split = (half << 8) | 2; r.part = part;
+        p.pairs[slot] = r;
+      }
+    } else {
+      const int32_t c = min(cost, kCostBins - 1);
+      const uint32_t slot = atomicAdd(&hist[c], 1u);
+      PairRec r;
+      r.b = b; r.row0 = row0; r.split = 1; r.part = -1;
+      p.pairs[slot] = r;
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -169,11 +213,12 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
       p.header[kHdrGroupStart + g] = acc;
       acc += group_count[g];
     }
-    p.header[kHdrGroupStart + kCostGroups] = acc;
+    p.header[kHdrGroupStart + kCostGroups] = acc;   // entries after splitting
     p.header[kHdrCounter] = 0u;
     p.header[kHdrStatus] = status_s;
-    p.header[kHdrNumPairs] = (uint32_t)total;
-    p.header[kHdrNumTiles] = (uint32_t)total * (uint32_t)p.h_q;
+    p.header[kHdrNumPairs] = acc;
+    p.header[kHdrNumTiles] = acc * (uint32_t)p.h_q;
+    p.header[kHdrNumSplit] = split_on ? n_splittable : 0u;
   }
 }
 

@@ -8,6 +8,7 @@ namespace thd {
 bool tc_kernel_available();
 int tc_rows_per_unit();   // query rows of one scheduled unit (two 128-row sub-tiles)
 int tc_keys_per_tile();   // keys per KV tile
+int tc_grid_size(int num_sms, int max_pairs, int h_q);  // persistent CTAs launched
 // Encodes the TMA descriptors for Q/K/V from the plan's strides and launches the
 // persistent kernel. Returns cudaErrorNotSupported when the descriptors cannot
 // be encoded for these pointers/strides.

@@ -26,7 +26,7 @@ def _strided(t: torch.Tensor, extra_heads: int, device) -> tuple[torch.Tensor, t
 
 
 def run_thd(batch: wl.ThdBatch, kernel: int = bd.KERNEL_AUTO, device="cuda", gaps=(0, 0, 0, 0),
-            stream=None, reps: int = 1):
+            stream=None, reps: int = 1, flags: int = 0):
     """Launch the forward pass; returns host copies of O (view), Stats, O backing,
     the status word and the plan."""
     q, qb = _strided(batch.q, gaps[0] * batch.h_q, device)
@@ -42,7 +42,7 @@ def run_thd(batch: wl.ThdBatch, kernel: int = bd.KERNEL_AUTO, device="cuda", gap
     mask = torch.from_numpy(np.ascontiguousarray(batch.mask_type, dtype=np.int8)).to(device)
     qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
     plan = bd.plan_for_tensors(q, k, v, o, batch.batch, batch.cap_s, batch.stats_layout,
-                               batch.softmax_scale, kernel)
+                               batch.softmax_scale, kernel, flags)
     ws = bd.alloc_workspace(plan, device)
     for _ in range(reps):
         bd.thd_attn_fwd(plan, q, k, v, o, stats, cu_q, cu_k, *offs, mask, qco, ws, stream)

@@ -50,8 +50,29 @@ def unit_order(starts, h_q: int, h_kv: int):
 BAD_LENGTH, BAD_OFFSET, BAD_MASK, TILE_OVERFLOW = 1, 2, 4, 8
 
 
+SPLIT_WAVES, MIN_SPLIT_COST = 4, 4
+
+
+def split_entries(pairs, h_q: int, num_ctas: int, max_split: int, allow_split: bool):
+    """Scheduled entries after the KV-split decision: list of (b, row0, half, halves,
+    cost) and the number of split pairs. Pairs visiting at least MIN_SPLIT_COST KV
+    tiles are halved when the launch has fewer than SPLIT_WAVES waves of units."""
+    splittable = [p for p in pairs if p[2] >= MIN_SPLIT_COST]
+    on = (allow_split and len(pairs) > 0 and len(pairs) * h_q < SPLIT_WAVES * num_ctas
+          and 0 < len(splittable) <= max_split)
+    out = []
+    for b, r, c in pairs:
+        if on and c >= MIN_SPLIT_COST:
+            out.append((b, r, 0, 2, min(c // 2, COST_BINS - 1)))
+            out.append((b, r, 1, 2, min(c - c // 2, COST_BINS - 1)))
+        else:
+            out.append((b, r, 0, 1, c))
+    return out, (len(splittable) if on else 0)
+
+
 def mirror(batch, rows_per_unit: int, keys_per_tile: int, max_pairs: int, caps=None):
-    """Expected (meta [B, 8] int32, pairs list of (b, row0, cost), status, num_pairs)."""
+    """Expected (meta [B, 8] int32, pairs list of (b, row0, cost), status, num_pairs).
+    Costs are the unclamped KV-tile counts clamped to the bucket range."""
     lq = batch.lens_q()
     lk = batch.lens_k()
     if caps is None:

@@ -106,28 +106,67 @@ def test_kv_interleaved_view_equals_contiguous(kernel):
     assert torch.equal(a["stats"].view(torch.int32), b["stats"].view(torch.int32))
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_schedule_matches_cpu_mirror(kernel):
-    batch = wl.mixed_gqa()
-    res = run_thd(batch, kernel=kernel)
+SCHEDULE_CASES = [
+    ("mixed_gqa", {}, bd.KERNEL_AUTO, 0),                      # many units: no split
+    ("mixed_gqa", {}, bd.KERNEL_SIMT, 0),
+    ("cp_chunks", dict(docs=2, k_len=2048, q_len=768, h=4), bd.KERNEL_AUTO, 0),   # split
+    ("cp_chunks", dict(docs=2, k_len=2048, q_len=768, h=4), bd.KERNEL_AUTO, bd.FLAG_NO_KV_SPLIT),
+]
+
+
+@pytest.mark.parametrize("name,kw,kernel,flags", SCHEDULE_CASES)
+def test_schedule_matches_cpu_mirror(name, kw, kernel, flags):
+    batch = wl.make(name, **kw)
+    res = run_thd(batch, kernel=kernel, flags=flags)
     plan = res["plan"]
     ws = res["ws"].cpu().numpy()
     hdr, meta_off, base_off, pairs_off = plan.workspace_layout
     header = ws[hdr:hdr + 128].view(np.uint32)
-    meta_exp, pairs_exp, status_exp, n_exp = schedule_mirror.mirror(
+    meta_exp, pairs_exp, status_exp, n_base = schedule_mirror.mirror(
         batch, plan.rows_per_unit, plan.keys_per_tile, plan.max_pairs)
+    num_ctas = min(torch.cuda.get_device_properties(0).multi_processor_count, 2 * plan.max_pairs * batch.h_q)
+    allow = plan.kernel == bd.KERNEL_TCGEN05 and not flags
+    max_split = min(plan.max_pairs, -(-4 * 160 // batch.h_q)) if allow else 0
+    entries, n_split = schedule_mirror.split_entries(pairs_exp, batch.h_q, num_ctas, max_split, allow)
+    n_exp = len(entries)
     assert header[1] == status_exp and header[2] == n_exp and header[3] == n_exp * batch.h_q
-    starts = schedule_mirror.group_starts(pairs_exp)
+    assert header[16] == n_split
+    starts = schedule_mirror.group_starts([(b, r, c) for b, r, _, _, c in entries])
     assert list(header[4:4 + len(starts)]) == starts
     meta = ws[meta_off:meta_off + 32 * batch.batch].view(np.int32).reshape(batch.batch, 8)
     assert np.array_equal(meta, meta_exp)
-    pairs = ws[pairs_off:pairs_off + 8 * n_exp].view(np.int32).reshape(n_exp, 2)
-    # same multiset of (b, row0); costs non-increasing along the list
-    cost = {(b, r): c for b, r, c in pairs_exp}
-    got = [tuple(int(x) for x in p) for p in pairs]
+    recs = ws[pairs_off:pairs_off + 16 * n_exp].view(np.int32).reshape(n_exp, 4)
+    # same multiset of (b, row0, half, halves); costs non-increasing along the list;
+    # the two halves of a split pair share one partial slot, slots are 0..n_split-1
+    cost = {(b, r, hf, hs): c for b, r, hf, hs, c in entries}
+    got = [(int(x[0]), int(x[1]), int(x[2]) >> 8, int(x[2]) & 0xFF) for x in recs]
     assert sorted(got) == sorted(cost)
-    costs = [cost[p] for p in got]
+    costs = [cost[g] for g in got]
     assert all(x >= y for x, y in zip(costs, costs[1:]))
+    parts = {}
+    for g, x in zip(got, recs):
+        if g[3] == 2:
+            parts.setdefault((g[0], g[1]), set()).add(int(x[3]))
+        else:
+            assert int(x[3]) == -1
+    assert all(len(v) == 1 for v in parts.values())
+    assert sorted(next(iter(v)) for v in parts.values()) == list(range(n_split))
+
+
+@pytest.mark.parametrize("name", ["cp_chunks", "mixed_gqa", "separate_padding"])
+def test_kv_split_matches_unsplit(name):
+    """The split path (two halves of each key range merged by log-sum-exp weights)
+    agrees with the unsplit path and with the oracle."""
+    batch = wl.make(name, **SMALL[name])
+    a = run_thd(batch)
+    b = run_thd(batch, flags=bd.FLAG_NO_KV_SPLIT)
+    assert a["status"] == 0 and b["status"] == 0
+    check_parity(batch, a)
+    check_parity(batch, b)
+    check_untouched(batch, a)
+    tol_o, tol_l = TOL[batch.dtype]
+    diff = torch.nan_to_num((a["o"].float() - b["o"].float()).abs(), nan=0.0)
+    assert float(diff.max()) <= tol_o
 
 
 @pytest.mark.parametrize("kernel", KERNELS)

@@ -46,7 +46,9 @@ def test_static_workspace_matches_workspace_entry(name, kw):
     d = _device_batch(batch, dev)
     o_ref = batch.o_init().to(dev)
     s_ref = batch.stats_init().to(dev)
-    plan = bd.plan_for_tensors(d["q"], d["k"], d["v"], o_ref, batch.batch, batch.cap_s, batch.stats_layout)
+    # the static array holds no partial results of split key ranges: plan without splitting
+    plan = bd.plan_for_tensors(d["q"], d["k"], d["v"], o_ref, batch.batch, batch.cap_s, batch.stats_layout,
+                               flags=bd.FLAG_NO_KV_SPLIT)
     assert plan.workspace_bytes <= bd.static_workspace_capacity()
     ws = bd.alloc_workspace(plan, dev)
     bd.thd_attn_fwd(plan, d["q"], d["k"], d["v"], o_ref, s_ref, *d["meta"], d["qco"], ws)
