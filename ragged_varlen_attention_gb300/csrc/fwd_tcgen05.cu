@@ -496,56 +496,70 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= lim) s[c][i] = __float_as_uint(-INFINITY);
         }
-        // row max: 8 independent chains of 3-input max
-        float acc[8];
+        // P against the running reference max m (base 2, scaled). Fast path: no
+        // row max at all; it is valid while every p stays <= 2^15 (fp16-safe), which
+        // holds if the row sum does (p >= 0). Slow path (the row's first visible
+        // tile, or a sum above 2^15, or a non-finite sum): take the tile max, move
+        // m if it rose by more than 8, rescale l and O, and recompute P.
+        auto compute_p = [&](float mref, float& rs_out) {
+          const uint64_t scale2 = ptx::f2_pack(sl2, sl2);
+          const uint64_t shift2 = ptx::f2_pack(-mref, -mref);
+          uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = fmaxf(__uint_as_float(s[0][q]), __uint_as_float(s[0][q + 8]));
+          for (int hp = 0; hp < 2; ++hp) {       // keys [64*hp, 64*hp+64) -> P columns [32*hp, 32*hp+32)
+            uint32_t pk[32];
 #pragma unroll
-        for (int i = 16; i < 128; i += 16)
+            for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            acc[q] = ptx::fmax3(acc[q], __uint_as_float(s[(i + q) >> 5][(i + q) & 31]),
-                                __uint_as_float(s[(i + q + 8) >> 5][(i + q + 8) & 31]));
-        const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
-                                    fmaxf(acc[6], acc[7]));
-        // reference max in the log2 domain; moved only when the tile max exceeds it
-        // by more than 8 (values of p stay below 2^8), so O is rescaled rarely
-        const float mt = mx * sl2;
-        const bool resc = mt > m + 8.0f;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ptx::ex2(m - mt);
-          m = mt;
-        }
-        l *= alpha;
-        const float mref = (m == -INFINITY) ? 0.f : m;
-        const uint64_t scale2 = ptx::f2_pack(sl2, sl2);
-        const uint64_t shift2 = ptx::f2_pack(-mref, -mref);
-        uint64_t sum2[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {         // keys [64*hp, 64*hp+64) -> P columns [32*hp, 32*hp+32)
-          uint32_t pk[32];
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int c = 2 * hp + c2;
-              float x0, x1;
-              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])),
-                                         scale2, shift2),
-                             x0, x1);
-              const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-              sum2[(i >> 1) & 3] = ptx::f2_add(sum2[(i >> 1) & 3], ptx::f2_pack(p0, p1));
-              pk[c2 * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
-            }
-          ptx::tmem_st32(tS + 32 * hp, pk);
-        }
-        {
+              for (int i = 0; i < 32; i += 2) {
+                const int c = 2 * hp + c2;
+                float x0, x1;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])),
+                                           scale2, shift2),
+                               x0, x1);
+                const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                sum2[(i >> 1) & 3] = ptx::f2_add(sum2[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+                pk[c2 * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
+              }
+            ptx::tmem_st32(tS + 32 * hp, pk);
+          }
           float a0, a1, b0, b1;
           ptx::f2_unpack(ptx::f2_add(sum2[0], sum2[1]), a0, a1);
           ptx::f2_unpack(ptx::f2_add(sum2[2], sum2[3]), b0, b1);
-          l += (a0 + a1) + (b0 + b1);
+          rs_out = (a0 + a1) + (b0 + b1);
+        };
+        float rs = 0.f;
+        bool slow = __any_sync(0xffffffffu, m == -INFINITY);
+        if (!slow) {
+          compute_p(m, rs);
+          slow = __any_sync(0xffffffffu, !(rs <= 32768.f));
         }
+        float alpha = 1.f;
+        bool resc = false;
+        if (slow) {
+          // row max: 8 independent chains of 3-input max
+          float acc[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaxf(__uint_as_float(s[0][q]), __uint_as_float(s[0][q + 8]));
+#pragma unroll
+          for (int i = 16; i < 128; i += 16)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              acc[q] = ptx::fmax3(acc[q], __uint_as_float(s[(i + q) >> 5][(i + q) & 31]),
+                                  __uint_as_float(s[(i + q + 8) >> 5][(i + q + 8) & 31]));
+          const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
+                                      fmaxf(acc[6], acc[7]));
+          // the reference max moves only when the tile max exceeds it by more than
+          // 8, so O is rescaled rarely and p stays below 2^8 right after a move
+          const float mt = mx * sl2;
+          resc = mt > m + 8.0f;
+          if (resc) {
+            alpha = ptx::ex2(m - mt);
+            m = mt;
+          }
+          compute_p(m == -INFINITY ? 0.f : m, rs);
+        }
+        l = l * alpha + rs;
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // O_t already holds PV of tiles < j (the commit of S_t(j) covered PV_t(j-1))
 #pragma unroll
