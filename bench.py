@@ -3,7 +3,8 @@
 Default workload: long-context context-parallel query chunks -- 2 documents of
 65536 keys, a 4096-row query chunk per document at causal offset k_len - q_len
 (bottom-right causal), h_q = h_kv = 16, d = 128, bf16, head-major LSE. One step
-is one ``thd_attn_fwd`` (setup kernel + attention kernel) over that batch.
+is one ``thd_attn_fwd`` over that batch: setup kernel, attention kernel and, on
+the tensor-core path, the kernel that merges split key ranges.
 
 Metric: TFLOP/s counted over unmasked score entries, 4 * d * N_visible (QK^T and
 PV, multiply-add = 2), summed over sequences and query heads.
@@ -64,6 +65,27 @@ def valid_bytes(batch) -> int:
     e = batch.q.element_size()
     tq, tk = int(batch.lens_q().sum()), int(batch.lens_k().sum())
     return (2 * tq * batch.h_q * batch.d + 2 * tk * batch.h_kv * batch.d) * e + 4 * tq * batch.h_q
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention-kernel launch from profiles/traffic.json, only while
+    the kernel sources still hash to what was profiled (else None)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"fwd_tc_kernel/{workload}")
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    try:
+        for rel in rec["sources"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -383,10 +405,11 @@ def main():
                      if peak_src == "measured" else "fallback 1.9 PFLOP/s",
                      "kernel": "attention kernel alone (CUDA events on its stream)",
                      "kernel_ms": kernel_ms, "launches": kernel_launches,
-                     "traffic": None},
+                     "traffic": recorded_traffic(args.workload) if plan.kernel == bd.KERNEL_TCGEN05 else None,
+                     "traffic_unit": "bytes per launch (ncu dram read+write)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": args.e2e_steps},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if plan.kernel == bd.KERNEL_TCGEN05 else 2) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
