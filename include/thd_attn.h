@@ -118,6 +118,12 @@ typedef struct {
  *   which evens out the last wave. The partial results live in the workspace, so
  *   splitting enlarges workspace_bytes; this flag keeps the workspace small. */
 enum { THD_FLAG_NO_KV_SPLIT = 1u << 0 };
+/* THD_FLAG_TEST_STALL: test hook for the bounded-wait path of the tensor-core
+ * kernel. The MMA-issuing thread waits on a barrier that nothing completes, gives
+ * up after 100 ms, sets THD_DEV_WAIT_TIMEOUT in the status word, and every CTA
+ * drains and returns. Outputs are undefined after such a call; the CUDA context
+ * stays usable. Never set it outside tests. */
+enum { THD_FLAG_TEST_STALL = 1u << 31 };
 
 typedef struct thd_attn_plan_s* thd_attn_plan_t;
 

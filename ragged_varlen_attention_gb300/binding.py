@@ -15,6 +15,7 @@ import torch
 STATS_TOKEN_MAJOR, STATS_HEAD_MAJOR = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05 = 0, 1, 2
 FLAG_NO_KV_SPLIT = 1
+FLAG_TEST_STALL = 1 << 31
 _DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 _STATUS = {0: "THD_OK", 1: "THD_ERR_INVALID_ARG", 2: "THD_ERR_UNSUPPORTED",
            3: "THD_ERR_ALIGNMENT", 4: "THD_ERR_CAPACITY", 5: "THD_ERR_WORKSPACE",

@@ -286,6 +286,7 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   fp.part_o = reinterpret_cast<float*>(ws + plan->ws_off[5]);
   fp.part_lse = reinterpret_cast<float*>(ws + plan->ws_off[6]);
   fp.rows_per_unit = plan->rows_per_unit;
+  fp.test_stall = (d.flags & THD_FLAG_TEST_STALL) ? 1 : 0;
 
   // a view with no rows has no TMA descriptor: the SIMT kernel serves that call
   // (it walks any unit size, so the plan's schedule geometry still applies)

@@ -66,8 +66,8 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 // barrier indices
 enum : int {
   B_Q_FULL = 0, B_Q_EMPTY = 2, B_S_FULL = 4, B_O_FULL = 6, B_SCHED_FULL = 8, B_SCHED_EMPTY = 10,
-  B_FINAL = 12, B_P_DONE = 14, B_O_READ = 16,
-  B_KV = 18  // then kStages "full" and kStages "empty" barriers
+  B_FINAL = 12, B_P_DONE = 14, B_O_READ = 16, B_STALL = 18,
+  B_KV = 20  // then kStages "full" and kStages "empty" barriers
 };
 
 template <int D>
@@ -105,7 +105,7 @@ struct Sync {
   uint32_t* status;
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
   // bounded wait for the phase of `parity` on barrier i; false on abort/timeout
-  __device__ __forceinline__ bool wait(int i, uint32_t parity) const {
+  __device__ __forceinline__ bool wait(int i, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) const {
     const uint32_t b = bar(i);
     // short spin of non-blocking probes (wake-up latency matters on the critical
     // path), then sleep-hinted blocking tries so long waits leave the issue slots
@@ -116,7 +116,7 @@ struct Sync {
     for (;;) {
       if (ptx::mbar_try_wait_sleep(b, parity, 20000u)) return true;
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, (uint32_t)THD_DEV_WAIT_TIMEOUT);
         return false;
@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       ptx::mbar_init(sy.bar(B_SCHED_EMPTY + t), 9);  // 8 softmax warps + the issuing thread
       ptx::mbar_init(sy.bar(B_FINAL + t), 1);
       ptx::mbar_init(sy.bar(B_P_DONE + t), 4);   // one arrival per warp of the sub-tile
+      ptx::mbar_init(sy.bar(B_STALL + t), 1);    // never arrived on (test hook)
       ptx::mbar_init(sy.bar(B_O_READ + t), 4);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -359,6 +360,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint32_t q_uses[2] = {0, 0}, p_waits[2] = {0, 0}, o_reads_seen[2] = {0, 0}, o_read_waits[2] = {0, 0};
       uint32_t kv_base = 0;
       bool issued_any = false, ok = true;
+      // test hook: a wait nothing completes, bounded at 100 ms, exercises the abort path
+      if (p.test_stall) ok = sy.wait(B_STALL, 0, 100000000ull);
       for (uint32_t it = 0; ok; ++it) {
         const int slot = (int)(it & 1u);
         if (!sy.wait(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;

@@ -105,6 +105,7 @@ struct FwdParams {
   float* part_o;            // [max_split][2][h_q][rows_per_unit][d] normalised partial O
   float* part_lse;          // [max_split][2][h_q][rows_per_unit] partial LSE, base 2
   int32_t rows_per_unit;
+  int32_t test_stall;       // test hook: see THD_FLAG_TEST_STALL
 };
 
 // Work id -> (pair index into the pair list, query head). Pairs are sorted by

@@ -230,3 +230,18 @@ def test_empty_batch_and_all_empty_sequences():
     res = run_thd(batch)
     assert res["status"] == 0
     check_untouched(batch, res)
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """A wait that nothing completes (test hook) ends in ~100 ms: the kernel sets the
+    timeout bit, drains and returns; the next call on the same context is correct."""
+    import time
+    batch = wl.make("cp_chunks", **SMALL["cp_chunks"])
+    t0 = time.time()
+    res = run_thd(batch, flags=bd.FLAG_TEST_STALL)
+    assert time.time() - t0 < 30
+    assert res["status"] & bd.DEV_WAIT_TIMEOUT
+    good = run_thd(batch)
+    assert good["status"] == 0
+    check_parity(batch, good)
+    check_untouched(batch, good)
