@@ -277,6 +277,7 @@ def main():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kv-split", action="store_true", help="plan with THD_FLAG_NO_KV_SPLIT")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -312,7 +313,8 @@ def main():
     o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     stats_host = torch.empty(stats.shape, dtype=stats.dtype).pin_memory()
     plan = bd.plan_for_tensors(dev["q"], dev["k"], dev["v"], o, batch.batch, batch.cap_s,
-                               batch.stats_layout, batch.softmax_scale, kernel)
+                               batch.stats_layout, batch.softmax_scale, kernel,
+                               bd.FLAG_NO_KV_SPLIT if args.no_kv_split else 0)
     ws = bd.alloc_workspace(plan, device)
     stream = torch.cuda.current_stream(device)
     small_inputs = valid_bytes(batch) <= 129e6
@@ -397,6 +399,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16" if batch.dtype == "bf16" else batch.dtype, "data": "synthetic",
         "config": {**config_block(args, batch),
                    "kernel": "tcgen05" if plan.kernel == bd.KERNEL_TCGEN05 else "simt",
+                   "kv_split_allowed": plan.kernel == bd.KERNEL_TCGEN05 and not args.no_kv_split,
                    "flop_per_step": flop_per_step},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
@@ -409,7 +412,7 @@ def main():
                      "traffic_unit": "bytes per launch (ncu dram read+write)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": args.e2e_steps},
-        "gpu_launches": (3 if plan.kernel == bd.KERNEL_TCGEN05 else 2) * args.steps,
+        "gpu_launches": (3 if plan.kernel == bd.KERNEL_TCGEN05 and not args.no_kv_split else 2) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
