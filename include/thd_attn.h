@@ -108,6 +108,8 @@ typedef struct {
   float softmax_scale;            /* NaN => 1/sqrt(d) */
   thd_kernel_t kernel;
   uint32_t flags;                 /* THD_FLAG_* bits */
+  int32_t offset_multiplier;      /* with THD_FLAG_ELEMENT_OFFSETS: factor applied on the device
+                                     to every offset (0 or 1: none) */
 } thd_attn_desc_t;
 
 /* Plan flags.
@@ -118,6 +120,16 @@ typedef struct {
  *   which evens out the last wave. The partial results live in the workspace, so
  *   splitting enlarges workspace_bytes; this flag keeps the workspace small. */
 enum { THD_FLAG_NO_KV_SPLIT = 1u << 0 };
+/* THD_FLAG_ELEMENT_OFFSETS: the five offset arrays hold ELEMENT offsets, the
+ * convention where a sequence's offset is its first row times the tensor's token
+ * stride (Stats: times the Stats token stride), optionally scaled by
+ * offset_multiplier (applied on the device, like a ragged-offset multiplier).
+ * The setup kernel divides each by the tensor's token stride; an offset that is
+ * not a whole number of rows sets THD_DEV_BAD_OFFSET and that sequence gets no
+ * work (cuDNN-frontend issue "THD lowering never reads the bound ragged offsets",
+ * the element-vs-byte convention and multiplier notes; NVIDIA/cudnn-frontend PR
+ * #462, "Not addressed here": ragged_offset == cum_token x stride[2]). */
+enum { THD_FLAG_ELEMENT_OFFSETS = 1u << 1 };
 /* THD_FLAG_TEST_STALL: test hook for the bounded-wait path of the tensor-core
  * kernel. The MMA-issuing thread waits on a barrier that nothing completes, gives
  * up after 100 ms, sets THD_DEV_WAIT_TIMEOUT in the status word, and every CTA

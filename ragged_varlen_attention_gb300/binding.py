@@ -15,6 +15,7 @@ import torch
 STATS_TOKEN_MAJOR, STATS_HEAD_MAJOR = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05 = 0, 1, 2
 FLAG_NO_KV_SPLIT = 1
+FLAG_ELEMENT_OFFSETS = 2
 FLAG_TEST_STALL = 1 << 31
 _DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 _STATUS = {0: "THD_OK", 1: "THD_ERR_INVALID_ARG", 2: "THD_ERR_UNSUPPORTED",
@@ -47,6 +48,7 @@ class ThdAttnDesc(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("kernel", ctypes.c_int),
         ("flags", ctypes.c_uint32),
+        ("offset_multiplier", ctypes.c_int32),
     ]
 
 
@@ -131,7 +133,7 @@ def _view_bytes(t: torch.Tensor) -> int:
 def make_desc(dtype: torch.dtype, batch: int, h_q: int, h_kv: int, d: int, cap_rows, stride_tok,
               stride_head, nbytes=(0, 0, 0, 0), cap_rows_stats: int = 0,
               stats_layout: int = STATS_TOKEN_MAJOR, softmax_scale: float | None = None,
-              kernel: int = KERNEL_AUTO, flags: int = 0) -> ThdAttnDesc:
+              kernel: int = KERNEL_AUTO, flags: int = 0, offset_multiplier: int = 0) -> ThdAttnDesc:
     desc = ThdAttnDesc()
     desc.dtype = _DTYPE_CODE[dtype]
     desc.batch, desc.h_q, desc.h_kv, desc.d = batch, h_q, h_kv, d
@@ -145,6 +147,7 @@ def make_desc(dtype: torch.dtype, batch: int, h_q: int, h_kv: int, d: int, cap_r
     desc.softmax_scale = math.nan if softmax_scale is None else float(softmax_scale)
     desc.kernel = int(kernel)
     desc.flags = int(flags)
+    desc.offset_multiplier = int(offset_multiplier)
     return desc
 
 
@@ -159,7 +162,8 @@ def thd_attn_plan(desc: ThdAttnDesc) -> ThdAttnPlan:
 
 
 def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: int,
-                     softmax_scale=None, kernel: int = KERNEL_AUTO, flags: int = 0) -> ThdAttnPlan:
+                     softmax_scale=None, kernel: int = KERNEL_AUTO, flags: int = 0,
+                     offset_multiplier: int = 0) -> ThdAttnPlan:
     """Build a plan from [rows, heads, d] tensor views (last dim contiguous)."""
     for t in (q, k, v, o):
         if t.dim() != 3 or t.stride(2) != 1:
@@ -167,7 +171,7 @@ def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: 
     desc = make_desc(q.dtype, batch, q.shape[1], k.shape[1], q.shape[2],
                      [t.shape[0] for t in (q, k, v, o)], [t.stride(0) for t in (q, k, v, o)],
                      [t.stride(1) for t in (q, k, v, o)], [_view_bytes(t) for t in (q, k, v, o)],
-                     cap_rows_stats, stats_layout, softmax_scale, kernel, flags)
+                     cap_rows_stats, stats_layout, softmax_scale, kernel, flags, offset_multiplier)
     return thd_attn_plan(desc)
 
 

@@ -85,6 +85,12 @@ thd_status_t thd_attn_plan(thd_attn_plan_t* out, const thd_attn_desc_t* desc, si
     if (d.cap_rows[i] < 0 || d.cap_rows[i] >= (int64_t(1) << 31)) return THD_ERR_INVALID_ARG;
     if (d.stride_tok[i] < 0 || d.stride_head[i] < 0 || d.bytes[i] < 0) return THD_ERR_INVALID_ARG;
   }
+  if (d.offset_multiplier < 0) return THD_ERR_INVALID_ARG;
+  if (d.flags & THD_FLAG_ELEMENT_OFFSETS) {
+    // element offsets are divided by the token strides on the device
+    for (int i = 0; i < 4; ++i)
+      if (d.stride_tok[i] <= 0) return THD_ERR_INVALID_ARG;
+  }
   float scale = d.softmax_scale;
   if (std::isnan(scale)) scale = 1.0f / std::sqrt((float)d.d);
   if (!std::isfinite(scale)) return THD_ERR_INVALID_ARG;
@@ -260,6 +266,10 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   sp.max_pairs = plan->max_pairs;
   sp.h_q = d.h_q;
   sp.allow_split = plan->allow_split;
+  sp.element_offsets = (d.flags & THD_FLAG_ELEMENT_OFFSETS) ? 1 : 0;
+  sp.offset_multiplier = d.offset_multiplier > 0 ? d.offset_multiplier : 1;
+  for (int i = 0; i < 4; ++i) sp.tok_stride[i] = d.stride_tok[i] > 0 ? d.stride_tok[i] : 1;
+  sp.tok_stride[4] = plan->stats_tok > 0 ? plan->stats_tok : 1;
   sp.max_split = plan->max_split;
   sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
   sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);

@@ -75,6 +75,9 @@ struct SetupParams {
   int32_t max_pairs;        // pairs before splitting
   int32_t h_q;
   int32_t allow_split;      // KV split permitted (workspace holds the partial buffers)
+  int32_t element_offsets;  // offsets are elements (x multiplier): divide by the token strides
+  int64_t offset_multiplier;
+  int64_t tok_stride[5];    // Q K V O Stats token strides (elements), for element offsets
   int32_t num_ctas;         // persistent CTAs of the attention kernel
   int32_t max_split;        // capacity of the split-pair table
   uint32_t* header;

@@ -93,10 +93,22 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
       const int32_t lk = p.cu_k[b + 1] - p.cu_k[b];
       SeqMeta m;
       m.len_q = lq; m.len_k = lk;
-      m.off_q = p.off_q[b]; m.off_k = p.off_k[b]; m.off_v = p.off_v[b];
-      m.off_o = p.off_o[b]; m.off_s = p.off_s[b];
-      const int mt = (int)p.mask[b];
       uint32_t bad = 0;
+      const int32_t* offs[5] = {p.off_q, p.off_k, p.off_v, p.off_o, p.off_s};
+      int32_t rows[5];
+#pragma unroll
+      for (int x = 0; x < 5; ++x) {
+        int64_t v = (int64_t)offs[x][b];
+        if (p.element_offsets) {
+          // element offset (x multiplier) -> row: must be a whole number of rows
+          v *= p.offset_multiplier;
+          if (v < 0 || v % p.tok_stride[x] != 0 || v / p.tok_stride[x] > 0x7fffffffll) bad |= THD_DEV_BAD_OFFSET;
+          v = v / p.tok_stride[x];
+        }
+        rows[x] = (int32_t)v;
+      }
+      m.off_q = rows[0]; m.off_k = rows[1]; m.off_v = rows[2]; m.off_o = rows[3]; m.off_s = rows[4];
+      const int mt = (int)p.mask[b];
       if (lq < 0 || lk < 0) bad |= THD_DEV_BAD_LENGTH;
       if (mt < 0 || mt > 2) bad |= THD_DEV_BAD_MASK;
       if (!bad) {

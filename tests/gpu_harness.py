@@ -26,9 +26,10 @@ def _strided(t: torch.Tensor, extra_heads: int, device) -> tuple[torch.Tensor, t
 
 
 def run_thd(batch: wl.ThdBatch, kernel: int = bd.KERNEL_AUTO, device="cuda", gaps=(0, 0, 0, 0),
-            stream=None, reps: int = 1, flags: int = 0):
+            stream=None, reps: int = 1, flags: int = 0, element_mult: int | None = None):
     """Launch the forward pass; returns host copies of O (view), Stats, O backing,
-    the status word and the plan."""
+    the status word and the plan. With ``element_mult`` the offsets are passed in
+    element units (row x token stride of each tensor, divided by the multiplier)."""
     q, qb = _strided(batch.q, gaps[0] * batch.h_q, device)
     k, kb = _strided(batch.k, gaps[1] * batch.h_kv, device)
     v, vb = _strided(batch.v, gaps[2] * batch.h_kv, device)
@@ -38,11 +39,25 @@ def run_thd(batch: wl.ThdBatch, kernel: int = bd.KERNEL_AUTO, device="cuda", gap
     stats = batch.stats_init().to(device)
     ints = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
     cu_q, cu_k = ints(batch.cu_seqlens_q), ints(batch.cu_seqlens_kv)
-    offs = [ints(x) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)]
+    row_offs = (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)
+    mult = 0
+    if element_mult is not None:
+        flags |= bd.FLAG_ELEMENT_OFFSETS
+        mult = element_mult
+        st_tok = batch.stats_strides[0]
+        strides = (q.stride(0), k.stride(0), v.stride(0), o.stride(0), st_tok)
+        div = max(1, element_mult)
+        conv = []
+        for off, sd in zip(row_offs, strides):
+            e = off.astype(np.int64) * sd
+            assert (e % div == 0).all()
+            conv.append(e // div)
+        row_offs = conv
+    offs = [ints(x) for x in row_offs]
     mask = torch.from_numpy(np.ascontiguousarray(batch.mask_type, dtype=np.int8)).to(device)
     qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
     plan = bd.plan_for_tensors(q, k, v, o, batch.batch, batch.cap_s, batch.stats_layout,
-                               batch.softmax_scale, kernel, flags)
+                               batch.softmax_scale, kernel, flags, mult)
     ws = bd.alloc_workspace(plan, device)
     for _ in range(reps):
         bd.thd_attn_fwd(plan, q, k, v, o, stats, cu_q, cu_k, *offs, mask, qco, ws, stream)

@@ -245,3 +245,40 @@ def test_bounded_wait_gives_up_and_context_survives():
     assert good["status"] == 0
     check_parity(batch, good)
     check_untouched(batch, good)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("mult", [0, 2, 4])
+def test_element_offsets_equal_row_offsets(kernel, mult):
+    """Offsets in element units (row x token stride, optionally divided by a
+    multiplier that the device applies back) give the same bits as row offsets,
+    with per-tensor token-stride gaps. Token-major Stats (token stride h_q = 4) keep
+    every element offset divisible by the multiplier."""
+    batch = wl.random_pack(300 + mult, batch=5, max_len=300, h_q=4, h_kv=2, d=64, dtype="bf16",
+                           stats_layout=wl.STATS_TOKEN_MAJOR)
+    gaps = (1, 2, 0, 3)
+    a = run_thd(batch, kernel=kernel, gaps=gaps)
+    b = run_thd(batch, kernel=kernel, gaps=gaps, element_mult=mult)
+    assert a["status"] == 0 and b["status"] == 0
+    assert torch.equal(a["o_backing"].view(torch.int16), b["o_backing"].view(torch.int16))
+    assert torch.equal(a["stats"].view(torch.int32), b["stats"].view(torch.int32))
+    check_parity(batch, b)
+
+
+def test_element_offset_not_a_whole_row_is_flagged():
+    batch = wl.random_pack(321, batch=3, max_len=100, h_q=2, h_kv=2, d=64, dtype="bf16", allow_empty=False)
+    res = run_thd(batch, element_mult=1)
+    assert res["status"] == 0
+    # shift sequence 1's K offset by one element: no longer a whole row
+    dev = res["dev"]
+    offs = [t.clone() for t in dev["offs"]]
+    offs[1][1] += 1
+    o = torch.empty_like(dev["o"])
+    o.view(torch.uint8).fill_(wl.SENTINEL_BYTE)
+    plan = res["plan"]
+    bd.thd_attn_fwd(plan, dev["q"], dev["k"], dev["v"], o, dev["stats"], dev["cu_q"], dev["cu_k"], *offs,
+                    dev["mask"], dev["qco"], res["ws"])
+    assert bd.thd_attn_read_status(plan, res["ws"]) == bd.DEV_BAD_OFFSET
+    # sequence 1's rows untouched, the others written
+    o1 = o.cpu().view(torch.uint8)[int(batch.off_o[1]):int(batch.off_o[1]) + int(batch.lens_q()[1])]
+    assert (o1 == wl.SENTINEL_BYTE).all()
