@@ -5,11 +5,11 @@ Imported by ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 """
 from .thd_attention import (MASK_CAUSAL_BOTTOM_RIGHT, MASK_CAUSAL_TOP_LEFT, MASK_NONE,
                             attention_one_head, causal_shift, thd_attention_fwd,
-                            unmasked_entries, visible_key_count)
+                            unmasked_entries, visible_key_count, window_lower_shift)
 from .brute import brute_attention
 
 __all__ = [
     "MASK_NONE", "MASK_CAUSAL_TOP_LEFT", "MASK_CAUSAL_BOTTOM_RIGHT", "attention_one_head",
     "causal_shift", "thd_attention_fwd", "unmasked_entries", "visible_key_count",
-    "brute_attention",
+    "brute_attention", "window_lower_shift",
 ]

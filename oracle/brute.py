@@ -10,7 +10,8 @@ numpy arithmetic), so the two agree only if both follow the definition:
 * row ``i`` sees key ``j < len_k`` when the mask is 0, ``j <= i`` when it is 1
   (top-left causal), ``j <= i + c`` when it is 2 (bottom-right causal, ``c`` the
   causal offset or ``len_k - len_q``), per TransformerEngine PR #3274 and
-  Megatron-LM PR #14;
+  Megatron-LM PR #14; with a left window ``w >= 0`` on a causal mask, also
+  ``j >= i + c - w`` (``c = 0`` for mask 1);
 * ``LSE_i`` is the natural log of the sum of ``exp`` of the scaled scores over the
   visible keys, ``O_i`` the probability-weighted sum of the visible values; a row
   with no visible key gets ``O_i = 0`` and ``LSE_i = -inf``.
@@ -23,7 +24,7 @@ import math
 
 
 def brute_attention(q, k, v, cu_q, cu_k, off_q, off_k, off_v, off_o, off_s, masks, qco,
-                    o_init, stats_init, stride_tok, stride_head, scale=None):
+                    o_init, stats_init, stride_tok, stride_head, scale=None, window_left=None):
     """Same contract as ``thd_attention_fwd`` but on nested Python lists.
 
     q/k/v/o_init: nested lists [rows][heads][d] of floats; stats_init: flat list.
@@ -48,11 +49,12 @@ def brute_attention(q, k, v, cu_q, cu_k, off_q, off_k, off_v, off_o, off_s, mask
                 for j in range(lk):
                     if masks[b] == 0:
                         ok = True
-                    elif masks[b] == 1:
-                        ok = j <= i
                     else:
-                        c = (lk - lq) if qco is None else qco[b]
+                        c = 0 if masks[b] == 1 else ((lk - lq) if qco is None else qco[b])
                         ok = j <= i + c
+                        w = None if window_left is None else window_left[b]
+                        if w is not None and w >= 0:
+                            ok = ok and j >= i + c - w
                     if ok:
                         krow = k[off_k[b] + j][g]
                         acc = 0.0

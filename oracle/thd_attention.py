@@ -22,7 +22,11 @@ time, in float64 with the inputs upcast exactly from their storage type:
     - 2 bottom-right causal:  ``j <= i + c`` with ``c = q_causal_offset[b]``
       (the key index of the chunk's local q[0]) or ``len_k - len_q`` when no
       offset tensor is given;
-  always with ``j < len_k``.
+  always with ``j < len_k``. An optional per-sequence left window ``w`` bounds the
+  causal masks from below (TransformerEngine PR #3274, "per-policy windows" /
+  ``window_size_per_mask_type`` for bounded causal attention): with mask 1 or 2
+  and ``w >= 0`` row ``i`` also needs ``j >= i + c - w`` (``c = 0`` for mask 1);
+  ``w < 0`` or mask 0 leaves it unbounded.
 * ``LSE_i = ln sum_{visible j} exp(s_ij)`` (natural log of the scaled scores,
   the FlashAttention / PyTorch-varlen ``softmax_lse`` convention referred to in
   cudnn-frontend PR #462, section "What");
@@ -66,19 +70,27 @@ def causal_shift(mask_type: int, len_q: int, len_k: int, q_causal_offset) -> int
     raise ValueError(f"unknown mask type {mask_type}")
 
 
-def visible_key_count(i: int, len_k: int, shift: int | None) -> int:
-    """Number of keys visible to query row ``i`` (keys ``0 .. count-1``)."""
-    if shift is None:
-        return len_k
-    return max(0, min(len_k, i + shift + 1))
+def window_lower_shift(mask_type: int, shift: int | None, window_left) -> int | None:
+    """Row ``i`` additionally needs ``j >= i + lower``; None when unbounded."""
+    if window_left is None or mask_type == MASK_NONE or int(window_left) < 0:
+        return None
+    return shift - int(window_left)
+
+
+def visible_key_count(i: int, len_k: int, shift: int | None, lower: int | None = None) -> int:
+    """Number of keys visible to query row ``i``."""
+    hi = len_k if shift is None else max(0, min(len_k, i + shift + 1))
+    lo = 0 if lower is None else max(0, i + lower)
+    return max(0, hi - lo)
 
 
 def attention_one_head(qb: np.ndarray, kb: np.ndarray, vb: np.ndarray, scale: float,
-                       shift: int | None, rows: slice | None = None):
+                       shift: int | None, rows: slice | None = None, lower: int | None = None):
     """O and LSE of one sequence and one query head, float64.
 
     ``qb`` [len_q, d], ``kb`` [len_k, d], ``vb`` [len_k, d_v]. ``rows``
-    restricts the evaluation to a subset of query rows (rows are independent).
+    restricts the evaluation to a subset of query rows (rows are independent);
+    ``lower`` is the window's lower shift (row i needs j >= i + lower).
     Returns ``(o [n, d_v], lse [n])``.
     """
     len_q, len_k = qb.shape[0], kb.shape[0]
@@ -94,6 +106,8 @@ def attention_one_head(qb: np.ndarray, kb: np.ndarray, vb: np.ndarray, scale: fl
         i_idx = np.arange(c0, c1)[:, None]
         j_idx = np.arange(len_k)[None, :]
         visible = np.ones_like(s, dtype=bool) if shift is None else (j_idx <= i_idx + shift)
+        if lower is not None:
+            visible &= j_idx >= i_idx + lower
         s = np.where(visible, s, -np.inf)
         row_max = s.max(axis=1)
         live = np.isfinite(row_max)
@@ -110,14 +124,14 @@ def attention_one_head(qb: np.ndarray, kb: np.ndarray, vb: np.ndarray, scale: fl
 
 def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v, off_o, off_s,
                       mask_type, q_causal_offset, o_init, stats_init, stats_stride_tok,
-                      stats_stride_head, softmax_scale=None, row_subset=None):
+                      stats_stride_head, softmax_scale=None, row_subset=None, window_left=None):
     """Forward attention over one packed THD batch.
 
     q [cap_q, h_q, d], k [cap_k, h_kv, d], v [cap_v, h_kv, d]: logical row views
     of the inputs (any float dtype; upcast to float64 exactly).
     o_init [cap_o, h_q, d] and stats_init (flat) are the output buffers' prior
     contents; copies are returned with the attention rows written.
-    ``q_causal_offset`` may be None. ``row_subset`` (optional) maps a sequence
+    ``q_causal_offset`` and ``window_left`` may be None. ``row_subset`` (optional) maps a sequence
     index to an iterable of query rows; only those rows are evaluated and
     written (rows are independent, so a subset is exact for those rows).
 
@@ -142,6 +156,8 @@ def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
         len_k = int(cu_seqlens_kv[b + 1]) - int(cu_seqlens_kv[b])
         shift = causal_shift(int(mask_type[b]), len_q, len_k,
                              None if q_causal_offset is None else q_causal_offset[b])
+        lower = window_lower_shift(int(mask_type[b]), shift,
+                                   None if window_left is None else window_left[b])
         qs, ks, vs = int(off_q[b]), int(off_k[b]), int(off_v[b])
         os_, ss = int(off_o[b]), int(off_s[b])
         rows = None
@@ -154,7 +170,7 @@ def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
             kb = k[ks:ks + len_k, g, :]
             vb = v[vs:vs + len_k, g, :]
             if rows is None:
-                ob, lb = attention_one_head(qb, kb, vb, scale, shift)
+                ob, lb = attention_one_head(qb, kb, vb, scale, shift, lower=lower)
                 idx = np.arange(len_q)
             else:
                 idx = np.array(rows, dtype=np.int64)
@@ -162,7 +178,7 @@ def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
                 lb = np.full((len(idx),), -np.inf)
                 for n, r in enumerate(idx):
                     ob[n:n + 1], lb[n:n + 1] = attention_one_head(qb, kb, vb, scale, shift,
-                                                                  rows=slice(r, r + 1))
+                                                                  rows=slice(r, r + 1), lower=lower)
             o[os_ + idx, h, :] = ob
             stats[(ss + idx) * stats_stride_tok + h * stats_stride_head] = lb
         if rows is None:
@@ -172,7 +188,8 @@ def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
     return o, stats, written
 
 
-def unmasked_entries(cu_seqlens_q, cu_seqlens_kv, mask_type, q_causal_offset, h_q) -> int:
+def unmasked_entries(cu_seqlens_q, cu_seqlens_kv, mask_type, q_causal_offset, h_q,
+                     window_left=None) -> int:
     """Count of visible score entries summed over sequences and query heads."""
     total = 0
     for b in range(len(cu_seqlens_q) - 1):
@@ -180,10 +197,14 @@ def unmasked_entries(cu_seqlens_q, cu_seqlens_kv, mask_type, q_causal_offset, h_
         len_k = int(cu_seqlens_kv[b + 1]) - int(cu_seqlens_kv[b])
         shift = causal_shift(int(mask_type[b]), len_q, len_k,
                              None if q_causal_offset is None else q_causal_offset[b])
+        lower = window_lower_shift(int(mask_type[b]), shift,
+                                   None if window_left is None else window_left[b])
         if shift is None:
             total += len_q * len_k
             continue
-        # rows i with 0 < i + shift + 1 < len_k see i + shift + 1 keys; clamp the rest
+        # row i sees keys [max(0, i + lower), min(len_k, i + shift + 1))
         i = np.arange(len_q, dtype=np.int64)
-        total += int(np.clip(i + shift + 1, 0, len_k).sum())
+        hi = np.clip(i + shift + 1, 0, len_k)
+        lo = np.zeros_like(i) if lower is None else np.clip(i + lower, 0, len_k)
+        total += int(np.maximum(hi - lo, 0).sum())
     return total * h_q

@@ -67,6 +67,7 @@ class ThdBatch:
     cap_o: int
     cap_s: int
     softmax_scale: float | None = None
+    window_left: np.ndarray | None = None   # int32 [B] or None
     notes: dict = field(default_factory=dict)
 
     @property
@@ -231,7 +232,8 @@ def make(name: str, seed: int | None = None, **kw) -> ThdBatch:
 def random_pack(seed: int, *, batch: int = 4, max_len: int = 200, h_q: int = 4, h_kv: int = 2,
                 d: int = 64, dtype: str = "bf16", max_gap: int = 9, stats_layout: int | None = None,
                 masks=(0, 1, 2), with_qco: bool | None = None, allow_empty: bool = True,
-                separate_kv_len: bool = True, nan_pads: bool = True) -> ThdBatch:
+                separate_kv_len: bool = True, nan_pads: bool = True,
+                with_window: bool = False) -> ThdBatch:
     """Small random pack for fuzzing: ragged lengths, per-tensor gaps, mixed masks.
 
     Q/O/Stats share one set of offsets and K/V another, each with its own random
@@ -265,6 +267,11 @@ def random_pack(seed: int, *, batch: int = 4, max_len: int = 200, h_q: int = 4, 
                        dtype=np.int32)
     if stats_layout is None:
         stats_layout = int(rng.integers(0, 2))
+    window = None
+    if with_window:
+        # unbounded (-1), zero, and windows shorter and longer than the sequence
+        window = np.array([int(rng.choice([-1, 0, int(rng.integers(1, max_len + 2)), 3 * max_len]))
+                           for _ in range(batch)], dtype=np.int32)
     return ThdBatch(f"random_pack_{seed}", dtype, h_q, h_kv, d, _cumsum0(lq), _cumsum0(lk),
                     off_q, off_k, off_k.copy(), off_q.copy(), off_q.copy(), mask, qco,
-                    stats_layout, q, k, v, cap_q, cap_q)
+                    stats_layout, q, k, v, cap_q, cap_q, window_left=window)

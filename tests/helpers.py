@@ -21,7 +21,8 @@ def oracle_on_batch(batch, o_init=None, stats_init=None, row_subset=None):
         batch.cu_seqlens_q, batch.cu_seqlens_kv, batch.off_q, batch.off_k, batch.off_v,
         batch.off_o, batch.off_s, batch.mask_type, batch.q_causal_offset,
         as_f64(o0), s0.to(torch.float64).numpy(), st_tok, st_head,
-        softmax_scale=batch.softmax_scale, row_subset=row_subset)
+        softmax_scale=batch.softmax_scale, row_subset=row_subset,
+        window_left=getattr(batch, "window_left", None))
 
 
 def written_stats_mask(batch) -> np.ndarray:

@@ -346,6 +346,86 @@ def pin_brute_force(seeds=range(20, 30)) -> float:
     return err
 
 
+def pin_window(seed=12) -> float:
+    """Left windows on causal masks: a window at least as long as the sequence changes
+    nothing; window 0 leaves exactly key i + c (O = v_{i+c}, LSE = its scaled score);
+    mask 0 ignores the window; every sequence equals torch SDPA under the explicit
+    band mask; the scalar loops agree."""
+    err = 0.0
+    bt = wl.random_pack(seed, batch=6, max_len=20, h_q=2, h_kv=1, d=8, dtype="fp32",
+                        nan_pads=False, with_qco=True, stats_layout=0, with_window=True)
+    q, k, v = as_f64(bt.q), as_f64(bt.k), as_f64(bt.v)
+    lq, lk = bt.lens_q(), bt.lens_k()
+    o0 = torch.zeros(bt.cap_o, bt.h_q, bt.d)
+    s0 = torch.zeros(bt.stats_numel)
+    # long windows == unbounded
+    long_w = dict(bt.__dict__)
+    long_w["window_left"] = np.full(bt.batch, 10 * 20, dtype=np.int32)
+    a, sa, _ = oracle_on_batch(wl.ThdBatch(**long_w), o_init=o0, stats_init=s0)
+    nw = dict(bt.__dict__)
+    nw["window_left"] = None
+    b_, sb, _ = oracle_on_batch(wl.ThdBatch(**nw), o_init=o0, stats_init=s0)
+    err = max(err, float(np.max(np.abs(a - b_))), max_abs_finite(sa, sb))
+    # window 0
+    zw = dict(bt.__dict__)
+    zw["window_left"] = np.zeros(bt.batch, dtype=np.int32)
+    oz, sz, _ = oracle_on_batch(wl.ThdBatch(**zw), o_init=o0, stats_init=s0)
+    scale = 1 / math.sqrt(bt.d)
+    for b in range(bt.batch):
+        c = _shift(int(bt.mask_type[b]), int(lq[b]), int(lk[b]),
+                   None if bt.q_causal_offset is None else bt.q_causal_offset[b])
+        for i in range(lq[b]):
+            for h in range(bt.h_q):
+                row, srow = bt.off_o[b] + i, (bt.off_s[b] + i) * bt.h_q + h
+                if c is None:                         # mask 0: unbounded, as without window
+                    err = max(err, float(np.max(np.abs(oz[row, h] - b_[row, h]))))
+                    continue
+                j = i + c
+                if 0 <= j < lk[b]:
+                    err = max(err, float(np.max(np.abs(oz[row, h] - v[bt.off_v[b] + j, 0]))))
+                    err = max(err, abs(sz[srow] - scale * float(q[bt.off_q[b] + i, h] @ k[bt.off_k[b] + j, 0])))
+                elif not (np.all(oz[row, h] == 0) and np.isneginf(sz[srow])):
+                    return float("inf")
+    # torch SDPA under the explicit band mask, rows with a visible key
+    o, st, _ = oracle_on_batch(bt, o_init=o0, stats_init=s0)
+    for b in range(bt.batch):
+        if lq[b] == 0 or lk[b] == 0:
+            continue
+        c = _shift(int(bt.mask_type[b]), int(lq[b]), int(lk[b]),
+                   None if bt.q_causal_offset is None else bt.q_causal_offset[b])
+        i = np.arange(lq[b])[:, None]
+        j = np.arange(lk[b])[None, :]
+        mb = np.ones((lq[b], lk[b]), dtype=bool) if c is None else (j <= i + c)
+        w = int(bt.window_left[b])
+        if c is not None and w >= 0:
+            mb &= j >= i + c - w
+        live = mb.any(axis=1)
+        for h in range(bt.h_q):
+            qb = q[bt.off_q[b]:bt.off_q[b] + lq[b], h]
+            kb = k[bt.off_k[b]:bt.off_k[b] + lk[b], 0]
+            vb = v[bt.off_v[b]:bt.off_v[b] + lk[b], 0]
+            od, ld = _dense_reference(qb, kb, vb, scale, mb)
+            rows = bt.off_o[b] + np.arange(lq[b])
+            srows = (bt.off_s[b] + np.arange(lq[b])) * bt.h_q + h
+            err = max(err, float(np.max(np.abs(o[rows, h][live] - od[live]), initial=0)))
+            err = max(err, float(np.max(np.abs(st[srows][live] - ld[live]), initial=0)))
+    # scalar loops
+    tiny = wl.random_pack(seed + 1, batch=3, max_len=7, h_q=2, h_kv=1, d=4, dtype="fp32",
+                          nan_pads=False, with_window=True)
+    ot, stt, _ = oracle_on_batch(tiny, o_init=torch.zeros(tiny.cap_o, 2, 4), stats_init=torch.zeros(tiny.stats_numel))
+    tok, head = tiny.stats_strides
+    ob, sb2 = brute_attention(as_f64(tiny.q).tolist(), as_f64(tiny.k).tolist(), as_f64(tiny.v).tolist(),
+                              [int(x) for x in tiny.cu_seqlens_q], [int(x) for x in tiny.cu_seqlens_kv],
+                              [int(x) for x in tiny.off_q], [int(x) for x in tiny.off_k],
+                              [int(x) for x in tiny.off_v], [int(x) for x in tiny.off_o],
+                              [int(x) for x in tiny.off_s], [int(x) for x in tiny.mask_type],
+                              None if tiny.q_causal_offset is None else [int(x) for x in tiny.q_causal_offset],
+                              np.zeros((tiny.cap_o, 2, 4)).tolist(), [0.0] * tiny.stats_numel, tok, head,
+                              window_left=[int(x) for x in tiny.window_left])
+    err = max(err, float(np.max(np.abs(np.array(ob) - ot))), max_abs_finite(np.array(sb2), stt))
+    return err
+
+
 PINS = {
     "identifier_layout": (pin_identifier_layout, 1e-12),
     "dense_special_case": (pin_dense_special_case, 1e-12),
@@ -355,6 +435,7 @@ PINS = {
     "closed_forms": (pin_closed_forms, 1e-12),
     "dead_rows": (pin_dead_rows, 0.0),
     "brute_force": (pin_brute_force, 1e-12),
+    "window": (pin_window, 1e-12),
 }
 
 
@@ -421,6 +502,14 @@ def _mutant_dead_row_nan(qb, kb, vb, scale, shift, rows=None):
     return o, lse
 
 
+_ORIG_LOWER = th.window_lower_shift
+
+
+def _mutant_window_off_by_one(mask_type, shift, window_left):
+    lo = _ORIG_LOWER(mask_type, shift, window_left)
+    return None if lo is None else lo + 1
+
+
 _ORIG_FWD = th.thd_attention_fwd
 
 
@@ -445,6 +534,7 @@ def _mutant_gqa_interleaved(q, k, v, *a, **kw):
     ("attention_one_head", _mutant_dead_row_nan),
     ("thd_attention_fwd", _mutant_offsets_from_prefix),
     ("thd_attention_fwd", _mutant_gqa_interleaved),
+    ("window_lower_shift", _mutant_window_off_by_one),
 ])
 def test_pins_catch_planted_mistakes(monkeypatch, target, mutant):
     """A mistake planted in the oracle (on the CPU) makes at least one pin fail."""
