@@ -56,7 +56,10 @@ def unmasked_entries(batch) -> int:
         shift = 0 if mt == 1 else (int(lk[b] - lq[b]) if batch.q_causal_offset is None
                                    else int(batch.q_causal_offset[b]))
         i = np.arange(int(lq[b]), dtype=np.int64)
-        total += int(np.clip(i + shift + 1, 0, int(lk[b])).sum())
+        hi = np.clip(i + shift + 1, 0, int(lk[b]))
+        w = -1 if batch.window_left is None else int(batch.window_left[b])
+        lo = np.clip(i + shift - w, 0, int(lk[b])) if w >= 0 else 0
+        total += int(np.maximum(hi - lo, 0).sum())
     return total * batch.h_q
 
 
@@ -186,7 +189,7 @@ def oracle_sample_time(batch, budget_s: float, max_rows: int | None = None):
     """Run the oracle on row slices of the workload until ``budget_s`` elapses.
 
     Returns (seconds, unmasked FLOPs computed, description)."""
-    from oracle import attention_one_head, causal_shift
+    from oracle import attention_one_head, causal_shift, window_lower_shift
     q = batch.q
     scale = 1.0 / math.sqrt(batch.d) if batch.softmax_scale is None else batch.softmax_scale
     lq, lk = batch.lens_q(), batch.lens_k()
@@ -201,6 +204,8 @@ def oracle_sample_time(batch, budget_s: float, max_rows: int | None = None):
             break
         shift = causal_shift(int(batch.mask_type[b]), int(lq[b]), int(lk[b]),
                              None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+        lower = window_lower_shift(int(batch.mask_type[b]), shift,
+                                   None if batch.window_left is None else batch.window_left[b])
         for r0 in range(0, int(lq[b]), rows_per_call):
             r1 = min(int(lq[b]), r0 + rows_per_call)
             for h in range(batch.h_q):
@@ -209,10 +214,15 @@ def oracle_sample_time(batch, budget_s: float, max_rows: int | None = None):
                 kb = batch.k[batch.off_k[b]:batch.off_k[b] + lk[b], g].to(torch.float64).numpy()
                 vb = batch.v[batch.off_v[b]:batch.off_v[b] + lk[b], g].to(torch.float64).numpy()
                 ts = time.perf_counter()
-                attention_one_head(qb, kb, vb, scale, shift, rows=slice(r0, r1))
+                attention_one_head(qb, kb, vb, scale, shift, rows=slice(r0, r1), lower=lower)
                 t_step = time.perf_counter() - ts
                 i = np.arange(r0, r1, dtype=np.int64)
-                n = (r1 - r0) * int(lk[b]) if shift is None else int(np.clip(i + shift + 1, 0, int(lk[b])).sum())
+                if shift is None:
+                    n = (r1 - r0) * int(lk[b])
+                else:
+                    hi = np.clip(i + shift + 1, 0, int(lk[b]))
+                    lo = 0 if lower is None else np.clip(i + lower, 0, int(lk[b]))
+                    n = int(np.maximum(hi - lo, 0).sum())
                 flops += 4 * batch.d * n
                 done.append(t_step)
                 if sum(done) >= budget_s or (max_rows is not None and len(done) * rows_per_call >= max_rows):
@@ -260,6 +270,7 @@ def config_block(args, batch):
             "batch": batch.batch, "h_q": batch.h_q, "h_kv": batch.h_kv, "d": batch.d,
             "tokens_q": int(batch.lens_q().sum()), "tokens_k": int(batch.lens_k().sum()),
             "unmasked_entries": unmasked_entries(batch),
+            "window_left": None if batch.window_left is None else int(batch.window_left[0]),
             "l2": "inputs larger than L2 (K/V alone exceed 129 MB); no flush between steps"
             if valid_bytes(batch) > 129e6 else "inputs smaller than L2; L2 flushed between timed steps",
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
@@ -278,11 +289,16 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kv-split", action="store_true", help="plan with THD_FLAG_NO_KV_SPLIT")
+    ap.add_argument("--window-left", type=int, default=None,
+                    help="left window (keys) on every causal sequence, through thd_attn_fwd_window")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     from ragged_varlen_attention_gb300 import workloads as wl
     batch = wl.make(args.workload)
+    if args.window_left is not None:
+        import dataclasses
+        batch = dataclasses.replace(batch, window_left=np.full(batch.batch, args.window_left, dtype=np.int32))
     if args.impl == "reference":
         run_reference(args, batch)
         return
@@ -305,7 +321,8 @@ def main():
             "offs": [ints(x).pin_memory() for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o,
                                                     batch.off_s)],
             "mask": ints(batch.mask_type, np.int8).pin_memory(),
-            "qco": None if batch.q_causal_offset is None else ints(batch.q_causal_offset).pin_memory()}
+            "qco": None if batch.q_causal_offset is None else ints(batch.q_causal_offset).pin_memory(),
+            "win": None if batch.window_left is None else ints(batch.window_left).pin_memory()}
     dev = {k: (None if v is None else ([t.to(device) for t in v] if isinstance(v, list) else v.to(device)))
            for k, v in host.items()}
     o = torch.zeros((batch.cap_o, batch.h_q, batch.d), dtype=batch.torch_dtype, device=device)
@@ -321,8 +338,8 @@ def main():
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device) if small_inputs else None
 
     def step():
-        bd.thd_attn_fwd(plan, dev["q"], dev["k"], dev["v"], o, stats, dev["cu_q"], dev["cu_k"], *dev["offs"],
-                        dev["mask"], dev["qco"], ws, stream)
+        bd.thd_attn_fwd_window(plan, dev["q"], dev["k"], dev["v"], o, stats, dev["cu_q"], dev["cu_k"],
+                               *dev["offs"], dev["mask"], dev["qco"], dev["win"], ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -366,12 +383,13 @@ def main():
     # end-to-end through the public API: pinned host inputs -> device -> fwd -> host outputs
     h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"], host["cu_q"],
                                                       host["cu_k"], host["mask"], *host["offs"]))
-    if host["qco"] is not None:
-        h2d += host["qco"].numel() * host["qco"].element_size()
+    for name in ("qco", "win"):
+        if host[name] is not None:
+            h2d += host[name].numel() * host[name].element_size()
     d2h = o_host.numel() * o_host.element_size() + stats_host.numel() * 4
 
     def e2e_step():
-        for name in ("q", "k", "v", "cu_q", "cu_k", "mask", "qco"):
+        for name in ("q", "k", "v", "cu_q", "cu_k", "mask", "qco", "win"):
             if host[name] is not None:
                 dev[name].copy_(host[name], non_blocking=True)
         for dt, ht in zip(dev["offs"], host["offs"]):

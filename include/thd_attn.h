@@ -166,6 +166,22 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
                           const int32_t* off_s, const int8_t* mask_type,
                           const int32_t* q_causal_offset, void* workspace, void* stream);
 
+/* thd_attn_fwd with a per-sequence left window on the causal masks.
+ *   window_left   device int32 [B] or NULL. For a sequence with mask 1 or 2 and
+ *                 window_left[b] = w >= 0, row i sees keys i + c - w .. i + c
+ *                 (c = 0 for mask 1; bounded causal attention); w < 0, mask 0 or
+ *                 NULL leave the lower end unbounded. TransformerEngine PR #3274
+ *                 describes per-policy windows for such bounded causal attention.
+ * All other arguments and results as in thd_attn_fwd, which equals this call with
+ * window_left = NULL. */
+thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void* k, const void* v,
+                                 void* o, float* stats, const int32_t* cu_seqlens_q,
+                                 const int32_t* cu_seqlens_kv, const int32_t* off_q,
+                                 const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
+                                 const int32_t* off_s, const int8_t* mask_type,
+                                 const int32_t* q_causal_offset, const int32_t* window_left,
+                                 void* workspace, void* stream);
+
 /* Copy the device status word of the last fwd on this workspace to *host_out and
  * synchronise `stream`. This is the only call that waits on the device. */
 thd_status_t thd_attn_read_status(thd_attn_plan_t plan, const void* workspace,

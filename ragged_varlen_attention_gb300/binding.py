@@ -56,7 +56,8 @@ _LIB = None
 _EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_plan_kernel",
             "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
             "thd_attn_status_string", "thd_attn_view_span_bytes", "thd_attn_profile_enable",
-            "thd_attn_profile_read", "thd_attn_fwd_static_ws", "thd_attn_static_workspace_capacity"]
+            "thd_attn_profile_read", "thd_attn_fwd_static_ws", "thd_attn_static_workspace_capacity",
+            "thd_attn_fwd_window"]
 
 
 def library_path() -> str:
@@ -78,6 +79,8 @@ def load_library():
     lib.thd_attn_plan.restype = ctypes.c_int
     lib.thd_attn_fwd.argtypes = [vp] * 17
     lib.thd_attn_fwd.restype = ctypes.c_int
+    lib.thd_attn_fwd_window.argtypes = [vp] * 18
+    lib.thd_attn_fwd_window.restype = ctypes.c_int
     lib.thd_attn_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.thd_attn_read_status.restype = ctypes.c_int
     lib.thd_attn_plan_kernel.argtypes = [vp]
@@ -197,6 +200,22 @@ def thd_attn_fwd(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_
         raise ThdAttnError(st, "thd_attn_fwd")
 
 
+def thd_attn_fwd_window(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q,
+                        off_k, off_v, off_o, off_s, mask_type, q_causal_offset, window_left,
+                        workspace, stream=None) -> None:
+    """Enqueue the forward pass with a per-sequence left window on the causal masks
+    (see ``thd_attn_fwd_window`` in include/thd_attn.h); ``window_left`` is a device
+    int32 [B] tensor or None."""
+    lib = load_library()
+    st = lib.thd_attn_fwd_window(ctypes.c_void_p(plan.handle), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                 _ptr(stats), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(off_q),
+                                 _ptr(off_k), _ptr(off_v), _ptr(off_o), _ptr(off_s), _ptr(mask_type),
+                                 _ptr(q_causal_offset), _ptr(window_left), _ptr(workspace),
+                                 _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_fwd_window")
+
+
 def thd_attn_fwd_static_ws(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q,
                            off_k, off_v, off_o, off_s, mask_type, q_causal_offset, stream=None) -> None:
     """Enqueue the forward pass with the library's static scratch array instead of a
@@ -253,12 +272,13 @@ _PLAN_CACHE: dict = {}
 def thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=None, off_v=None,
                      off_o=None, off_s=None, mask_type=None, q_causal_offset=None, o=None,
                      stats=None, stats_layout: int = STATS_TOKEN_MAJOR, softmax_scale=None,
-                     kernel: int = KERNEL_AUTO, workspace=None, stream=None):
+                     kernel: int = KERNEL_AUTO, workspace=None, stream=None, window_left=None):
     """One-call forward over device tensors.
 
     Offsets default to the cu_seqlens arrays (packed layout); ``mask_type``
     defaults to no mask. O and Stats are allocated when not given (O with the
-    shape of Q; Stats with Q's rows). Returns ``(o, stats)``.
+    shape of Q; Stats with Q's rows). ``window_left`` (device int32 [B]) bounds
+    the causal masks from the left. Returns ``(o, stats)``.
     """
     batch = cu_seqlens_q.numel() - 1
     dev = q.device
@@ -283,6 +303,6 @@ def thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=
         _PLAN_CACHE[key] = plan
     if workspace is None:
         workspace = alloc_workspace(plan, dev)
-    thd_attn_fwd(plan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v, off_o,
-                 off_s, mask_type, q_causal_offset, workspace, stream)
+    thd_attn_fwd_window(plan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
+                        off_o, off_s, mask_type, q_causal_offset, window_left, workspace, stream)
     return o, stats

@@ -239,6 +239,15 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
                           const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
                           const int32_t* off_s, const int8_t* mask, const int32_t* qco, void* workspace,
                           void* stream_ptr) {
+  return thd_attn_fwd_window(plan, q, k, v, o, stats, cu_q, cu_k, off_q, off_k, off_v, off_o, off_s, mask, qco,
+                             nullptr, workspace, stream_ptr);
+}
+
+thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                                 float* stats, const int32_t* cu_q, const int32_t* cu_k, const int32_t* off_q,
+                                 const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
+                                 const int32_t* off_s, const int8_t* mask, const int32_t* qco,
+                                 const int32_t* window_left, void* workspace, void* stream_ptr) {
   if (!plan) return THD_ERR_INVALID_ARG;
   const thd_attn_desc_t& d = plan->desc;
   if (!workspace) return THD_ERR_WORKSPACE;
@@ -257,7 +266,7 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   thd::SetupParams sp;
   sp.cu_q = cu_q; sp.cu_k = cu_k;
   sp.off_q = off_q; sp.off_k = off_k; sp.off_v = off_v; sp.off_o = off_o; sp.off_s = off_s;
-  sp.mask = mask; sp.qco = qco;
+  sp.mask = mask; sp.qco = qco; sp.window = window_left;
   sp.cap_q = d.cap_rows[0]; sp.cap_k = d.cap_rows[1]; sp.cap_v = d.cap_rows[2]; sp.cap_o = d.cap_rows[3];
   sp.cap_s = d.cap_rows_stats;
   sp.batch = d.batch;
@@ -297,6 +306,7 @@ thd_status_t thd_attn_fwd(thd_attn_plan_t plan, const void* q, const void* k, co
   fp.part_lse = reinterpret_cast<float*>(ws + plan->ws_off[6]);
   fp.rows_per_unit = plan->rows_per_unit;
   fp.test_stall = (d.flags & THD_FLAG_TEST_STALL) ? 1 : 0;
+  fp.has_window = window_left != nullptr ? 1 : 0;
 
   // a view with no rows has no TMA descriptor: the SIMT kernel serves that call
   // (it walks any unit size, so the plan's schedule geometry still applies)

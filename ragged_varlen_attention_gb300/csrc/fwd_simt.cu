@@ -87,11 +87,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdParams p, int row
       // keys this row may see: j < kmax_row
       const int64_t kmax_row64 = min64((int64_t)m.len_k, (int64_t)r + m.shift + 1);
       const int kmax_row = (int)max64(0, kmax_row64);
-      // keys any row of the unit may see
+      // lowest key this row may see (window), and the key range any row of the block may see
+      const int64_t kmin_row = (int64_t)r + m.lo_shift;
       const int64_t r_last = min64((int64_t)m.len_q, (int64_t)pr.row0 + sub + ROWS) - 1;
       const int kmax_unit = (int)max64(0, min64((int64_t)m.len_k, r_last + m.shift + 1));
+      const int kmin_unit = (int)min64((int64_t)kmax_unit, max64(0, (int64_t)pr.row0 + sub + m.lo_shift));
 
-      for (int j0 = 0; j0 < kmax_unit; j0 += kBN) {
+      for (int j0 = kmin_unit / kBN * kBN; j0 < kmax_unit; j0 += kBN) {
         // stage K/V rows j0 .. j0+kBN-1 (zeros past len_k)
         for (int idx = tid; idx < kBN * DMAX; idx += kThreads) {
           const int jj = idx / DMAX, e = idx % DMAX;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdParams p, int row
 #pragma unroll
           for (int e = 0; e < kDPT; ++e) a = fmaf(q[e], ks[jj][dbase + e], a);
           if (TPR == 2) a += __shfl_xor_sync(0xffffffffu, a, 1);
-          s[jj] = (j0 + jj < kmax_row) ? a : -INFINITY;
+          s[jj] = (j0 + jj < kmax_row && j0 + jj >= kmin_row) ? a : -INFINITY;
           tmax = fmaxf(tmax, s[jj]);
         }
         const float mnew = fmaxf(mrow, tmax);

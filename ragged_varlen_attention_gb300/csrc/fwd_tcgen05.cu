@@ -80,7 +80,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   static constexpr int kNumBars = B_KV + 2 * kStages;
   static constexpr int kOffInfo = kOffBar + kNumBars * 8;
-  static constexpr int kOffMisc = kOffInfo + 2 * 80;   // two UnitInfo slots
+  static constexpr int kOffMisc = kOffInfo + 2 * 96;   // two UnitInfo slots
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kColS = 0;
   static constexpr int kColO = 256;
@@ -90,14 +90,16 @@ struct Cfg {
 struct UnitInfo {
   uint32_t w;            // work id; >= num_tiles: no more work
   int32_t b, row0, h, g;
-  int32_t len_k, off_q, off_k, off_v, off_o, off_s, shift;
+  int32_t len_k, off_q, off_k, off_v, off_o, off_s, shift, lo_shift;
   int32_t n_kv[2];       // KV tiles each sub-tile visits in this entry
+  int32_t t_lo[2];       // loop index of each sub-tile's first tile (when n_kv > 0)
   int32_t n_rows[2];     // valid query rows of each sub-tile
-  int32_t kv_lo;         // first KV tile of this entry (0 unless the second half of a split)
+  int32_t kv_lo;         // absolute KV tile of loop index 0
+  int32_t n_tiles;       // KV tiles loaded for this entry
   int32_t part_slot;     // partial-result slot (2 * part + half), -1 for a whole pair
   int32_t pad[2];
 };
-static_assert(sizeof(UnitInfo) == 80, "UnitInfo is 80 bytes");
+static_assert(sizeof(UnitInfo) == 96, "UnitInfo is 96 bytes");
 
 struct Sync {
   uint32_t bar0;               // shared address of barrier 0
@@ -146,9 +148,9 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
   UnitInfo u;
   u.w = w;
   u.b = u.row0 = u.h = u.g = 0;
-  u.len_k = u.off_q = u.off_k = u.off_v = u.off_o = u.off_s = u.shift = 0;
-  u.n_kv[0] = u.n_kv[1] = u.n_rows[0] = u.n_rows[1] = 0;
-  u.kv_lo = 0;
+  u.len_k = u.off_q = u.off_k = u.off_v = u.off_o = u.off_s = u.shift = u.lo_shift = 0;
+  u.n_kv[0] = u.n_kv[1] = u.t_lo[0] = u.t_lo[1] = u.n_rows[0] = u.n_rows[1] = 0;
+  u.kv_lo = u.n_tiles = 0;
   u.part_slot = -1;
   u.pad[0] = u.pad[1] = 0;
   if (w >= num_tiles) return u;
@@ -163,35 +165,53 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
   u.len_k = m.len_k;
   u.off_q = m.off_q; u.off_k = m.off_k; u.off_v = m.off_v; u.off_o = m.off_o; u.off_s = m.off_s;
   u.shift = m.shift;
-  int full[2];
+  u.lo_shift = m.lo_shift;
+  // absolute KV tile range [first, end) of each sub-tile: from the tile holding
+  // its first row's lowest visible key to the one holding its last row's highest
+  int first[2], end[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r_begin = pr.row0 + t * BM;
     const int rows = max(0, min(BM, m.len_q - r_begin));
     u.n_rows[t] = rows;
-    int n = 0;
+    first[t] = (int)(max64(0, (int64_t)r_begin + m.lo_shift) / BN);
+    end[t] = 0;
     if (rows > 0) {
       const int64_t kmax = min64((int64_t)m.len_k, (int64_t)(r_begin + rows - 1) + m.shift + 1);
-      n = kmax > 0 ? (int)((kmax + BN - 1) / BN) : 0;
+      end[t] = kmax > 0 ? (int)((kmax + BN - 1) / BN) : 0;
     }
-    full[t] = n;
   }
-  // a split pair covers KV tiles [0, n/2) in its first half and [n/2, n) in its second
-  const int n_pair = max(full[0], full[1]);
+  // the pair spans [first[0], max end); a split pair covers the lower half of that
+  // span in its first half and the rest in its second
+  const int f_pair = first[0];
+  const int n_pair = max(0, max(end[0], end[1]) - f_pair);
   const int halves = pr.split & 0xff, half = pr.split >> 8;
-  int lo = 0, hi = n_pair;
+  int lo = f_pair, hi = f_pair + n_pair;
   if (halves == 2) {
-    lo = half == 0 ? 0 : n_pair / 2;
-    hi = half == 0 ? n_pair / 2 : n_pair;
+    lo = f_pair + (half == 0 ? 0 : n_pair / 2);
+    hi = f_pair + (half == 0 ? n_pair / 2 : n_pair);
     u.part_slot = 2 * pr.part + half;
   }
-  u.kv_lo = lo;
+  int start[2], kv_lo = hi;
 #pragma unroll
-  for (int t = 0; t < 2; ++t) u.n_kv[t] = max(0, min(hi, full[t]) - lo);
+  for (int t = 0; t < 2; ++t) {
+    start[t] = max(lo, first[t]);
+    u.n_kv[t] = max(0, min(hi, end[t]) - start[t]);
+    if (u.n_kv[t] > 0) kv_lo = min(kv_lo, start[t]);
+  }
+  u.kv_lo = kv_lo;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    u.t_lo[t] = u.n_kv[t] > 0 ? start[t] - kv_lo : 0;
+    if (u.n_kv[t] > 0) u.n_tiles = max(u.n_tiles, u.t_lo[t] + u.n_kv[t]);
+  }
   return u;
 }
 
-template <int D, bool BF16>
+// WIN: some sequence may carry a left window, so a sub-tile's KV range may start
+// after the unit's first tile (compiled out otherwise; the window-free variant keeps
+// the shorter issue loop and mask)
+template <int D, bool BF16, bool WIN>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -270,7 +290,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             ptx::tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + hf * BM * 128, &tm_q, qbar, hf * 64, u.h,
                              u.off_q + u.row0 + t * BM);
         }
-        const int n_tiles = max(u.n_kv[0], u.n_kv[1]);
+        const int n_tiles = u.n_tiles;
         for (int j = 0; j < n_tiles && ok; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
@@ -360,6 +380,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint32_t q_uses[2] = {0, 0}, p_waits[2] = {0, 0}, o_reads_seen[2] = {0, 0}, o_read_waits[2] = {0, 0};
       uint32_t kv_base = 0;
       bool issued_any = false, ok = true;
+      // first QK of sub-tile t (its S_t(start)) on the K tile in `kstage`
+      auto first_qk = [&](int t, int kstage, int n) -> bool {
+        if (!sy.wait(B_Q_FULL + t, (q_uses[t]++) & 1u)) return false;
+        ptx::tc_fence_after();
+        issue_qk(t, kstage);
+        ptx::tc_commit(sy.bar(B_S_FULL + t));
+        if (n == 1) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
+        return true;
+      };
       // test hook: a wait nothing completes, bounded at 100 ms, exercises the abort path
       if (p.test_stall) ok = sy.wait(B_STALL, 0, 100000000ull);
       for (uint32_t it = 0; ok; ++it) {
@@ -368,20 +397,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const UnitInfo u = info[slot];
         ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
         if (u.w >= num_tiles) break;
+        // sub-tile t visits loop indices [tl[t], te[t]); with a left window the
+        // second sub-tile may start later than the first
         const int nt[2] = {u.n_kv[0], u.n_kv[1]};
-        const int n_tiles = max(nt[0], nt[1]);
+        const int tl[2] = {WIN ? u.t_lo[0] : 0, WIN ? u.t_lo[1] : 0};
+        const int te[2] = {tl[0] + nt[0], tl[1] + nt[1]};
+        const int n_tiles = u.n_tiles;
         if (n_tiles == 0) continue;
         ok = sy.wait(B_KV + kv_stage(kv_base), kv_phase(kv_base));
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || nt[t] == 0) continue;
-          ok = sy.wait(B_Q_FULL + t, (q_uses[t]++) & 1u);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          issue_qk(t, kv_stage(kv_base));
-          ptx::tc_commit(sy.bar(B_S_FULL + t));
-          if (nt[t] == 1) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
-        }
+        for (int t = 0; t < 2; ++t)
+          if (ok && nt[t] > 0 && (!WIN || tl[t] == 0)) ok = first_qk(t, kv_stage(kv_base), nt[t]);
         if (!ok) break;
         ptx::tc_commit(sy.bar(B_KV + C::kStages + kv_stage(kv_base)));
         issued_any = true;
@@ -413,21 +439,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (!ok || j >= nt[t]) continue;
-            // the previous unit's epilogue has read O_t before PV_t(0) overwrites it
-            while (ok && j == 0 && o_read_waits[t] < o_reads_seen[t])
+            if (!ok || j < tl[t] || j >= te[t]) continue;
+            // the previous unit's epilogue has read O_t before the first PV_t overwrites it
+            while (ok && j == tl[t] && o_read_waits[t] < o_reads_seen[t])
               ok = sy.wait(B_O_READ + t, (o_read_waits[t]++) & 1u);
             ok = ok && sy.wait(B_P_DONE + t, (p_waits[t]++) & 1u);
             if (!ok) break;
             ptx::tc_fence_after();
-            issue_pv(t, vstage, j > 0, nk);
-            if (j + 1 < nt[t]) {
+            issue_pv(t, vstage, j > tl[t], nk);
+            if (j + 1 < te[t]) {
               issue_qk(t, kstage);
               ptx::tc_commit(sy.bar(B_S_FULL + t));
-              if (j + 2 == nt[t]) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
+              if (j + 2 == te[t]) ptx::tc_commit(sy.bar(B_Q_EMPTY + t));
             } else {
               ptx::tc_commit(sy.bar(B_O_FULL + t));
             }
+          }
+          if constexpr (WIN) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              if (ok && kmore && nt[t] > 0 && tl[t] == j + 1) ok = first_qk(t, kstage, nt[t]);
           }
           if (!ok) break;
           ptx::tc_commit(sy.bar(B_KV + C::kStages + vstage));
@@ -481,6 +512,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int r = u.row0 + t * BM + row;      // row inside the sequence
       const bool live = row < nrows;
       const int kmax_row = (int)max64(0, min64((int64_t)u.len_k, (int64_t)r + u.shift + 1));
+      const int kmin_row = WIN ? (int)max64(0, min64((int64_t)u.len_k, (int64_t)r + u.lo_shift)) : 0;
+      const int jt0 = u.kv_lo + (WIN ? (t ? u.t_lo[1] : u.t_lo[0]) : 0);   // absolute tile of j = 0
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
@@ -491,13 +524,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld(s[c]);
-        const int lim = kmax_row - (u.kv_lo + j) * BN;   // columns >= lim are not visible
+        const int lim = kmax_row - (jt0 + j) * BN;      // columns >= lim are not visible
         if (lim < BN) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= lim) s[c][i] = __float_as_uint(-INFINITY);
+        }
+        const int lim_lo = kmin_row - (jt0 + j) * BN;   // nor columns < lim_lo (left window)
+        if (WIN && lim_lo > 0) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i < lim_lo) s[c][i] = __float_as_uint(-INFINITY);
         }
         // P against the running reference max m (base 2, scaled). Fast path: no
         // row max at all; it is valid while every p stays <= 2^15 (fp16-safe), which
@@ -672,7 +713,7 @@ bool encode_view(CUtensorMap* map, const void* base, bool bf16, int d, int64_t h
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool WIN>
 cudaError_t launch_impl(const FwdParams& p, const thd_attn_desc_t& desc, int max_pairs, int num_sms,
                         cudaStream_t stream) {
   using C = Cfg<D>;
@@ -682,10 +723,10 @@ cudaError_t launch_impl(const FwdParams& p, const thd_attn_desc_t& desc, int max
       !encode_view(&tv, p.v, BF16, D, desc.h_kv, desc.cap_rows[2], desc.stride_head[2], desc.stride_tok[2]))
     return cudaErrorNotSupported;
   const int smem = C::kSmemBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = tc_grid_size(num_sms, max_pairs, desc.h_q);
-  fwd_tc_kernel<D, BF16><<<grid, kThreadsTC, smem, stream>>>(tq, tk, tv, p);
+  fwd_tc_kernel<D, BF16, WIN><<<grid, kThreadsTC, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -702,14 +743,19 @@ int tc_keys_per_tile() { return BN; }
 cudaError_t launch_fwd_tc(const FwdParams& p, const thd_attn_desc_t& desc, int max_pairs, int num_sms,
                           cudaStream_t stream) {
   const bool bf16 = desc.dtype == THD_BF16;
+  const bool win = p.has_window != 0;
+#define THD_TC_LAUNCH(D_, B_)                                                     \
+  return win ? launch_impl<D_, B_, true>(p, desc, max_pairs, num_sms, stream)     \
+             : launch_impl<D_, B_, false>(p, desc, max_pairs, num_sms, stream)
   if (desc.d == 128) {
-    return bf16 ? launch_impl<128, true>(p, desc, max_pairs, num_sms, stream)
-                : launch_impl<128, false>(p, desc, max_pairs, num_sms, stream);
+    if (bf16) THD_TC_LAUNCH(128, true);
+    THD_TC_LAUNCH(128, false);
   }
   if (desc.d == 64) {
-    return bf16 ? launch_impl<64, true>(p, desc, max_pairs, num_sms, stream)
-                : launch_impl<64, false>(p, desc, max_pairs, num_sms, stream);
+    if (bf16) THD_TC_LAUNCH(64, true);
+    THD_TC_LAUNCH(64, false);
   }
+#undef THD_TC_LAUNCH
   return cudaErrorNotSupported;
 }
 

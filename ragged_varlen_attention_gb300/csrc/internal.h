@@ -35,11 +35,13 @@ constexpr int kMaxSmsForSizing = 160;
 
 // Per-sequence record written by the setup kernel. `shift` is the causal shift:
 // query row i sees keys j < len_k with j <= i + shift (mask 0 stores len_k, which
-// lets every key through for any i >= 0).
+// lets every key through for any i >= 0); `lo_shift` the window's lower end:
+// also j >= i + lo_shift (kNoLowerBound when unbounded).
 struct SeqMeta {
-  int32_t len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift;
+  int32_t len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift, lo_shift, pad[3];
 };
-static_assert(sizeof(SeqMeta) == 32, "SeqMeta is 32 bytes");
+static_assert(sizeof(SeqMeta) == 48, "SeqMeta is 48 bytes");
+constexpr int32_t kNoLowerBound = -(1 << 30);
 
 // A scheduled unit: rows [row0, row0 + rows_per_unit) of sequence b, for every
 // query head. `split` = (half << 8) | halves: halves is 1 for a whole pair, 2 when
@@ -68,6 +70,7 @@ struct SetupParams {
   const int32_t* off_s;
   const int8_t* mask;
   const int32_t* qco;       // may be null
+  const int32_t* window;    // may be null
   int64_t cap_q, cap_k, cap_v, cap_o, cap_s;
   int32_t batch;
   int32_t rows_per_unit;
@@ -109,6 +112,7 @@ struct FwdParams {
   float* part_lse;          // [max_split][2][h_q][rows_per_unit] partial LSE, base 2
   int32_t rows_per_unit;
   int32_t test_stall;       // test hook: see THD_FLAG_TEST_STALL
+  int32_t has_window;       // a window tensor was passed (some lo_shift may be bounded)
 };
 
 // Work id -> (pair index into the pair list, query head). Pairs are sorted by

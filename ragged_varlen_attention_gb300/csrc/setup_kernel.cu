@@ -48,13 +48,16 @@ __device__ __forceinline__ int32_t block_inclusive_scan(int32_t x, int32_t* warp
   return r;
 }
 
-// number of KV tiles the pair starting at row0 must visit (max over its rows)
+// number of KV tiles the pair starting at row0 must visit: from the tile of the
+// first row's lowest visible key to the tile of the last row's highest
 __device__ __forceinline__ int32_t pair_cost(const SeqMeta& m, int32_t row0, int32_t rows_per_unit,
                                              int32_t keys_per_tile) {
   const int64_t r_end = min64((int64_t)m.len_q, (int64_t)row0 + rows_per_unit);
   const int64_t kmax = min64((int64_t)m.len_k, r_end + (int64_t)m.shift);
   if (kmax <= 0) return 0;
-  return (int32_t)((kmax + keys_per_tile - 1) / keys_per_tile);
+  const int64_t kmin = max64(0, (int64_t)row0 + (int64_t)m.lo_shift);
+  const int64_t first = kmin / keys_per_tile, end = (kmax + keys_per_tile - 1) / keys_per_tile;
+  return (int32_t)max64(0, end - first);
 }
 
 // group of a (clamped) cost: 0 for 512..1023, 1 for 256..511, ..., 9 for 1, 10 for 0
@@ -124,9 +127,15 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
       if (mt == THD_MASK_NONE) shift = lk;
       else if (mt == THD_MASK_CAUSAL_TOP_LEFT) shift = 0;
       else shift = p.qco ? (int64_t)p.qco[b] : (int64_t)lk - (int64_t)lq;
+      // left window of the causal masks: row i also needs j >= i + shift - w
+      int64_t lo = kNoLowerBound;
+      if (p.window && mt != THD_MASK_NONE && p.window[b] >= 0) lo = shift - (int64_t)p.window[b];
       // beyond +-2^30 a shift no longer changes which keys are visible
       shift = max64(-(1ll << 30), min64(1ll << 30, shift));
+      lo = max64(kNoLowerBound, min64(1ll << 30, lo));
       m.shift = (int32_t)shift;
+      m.lo_shift = (int32_t)lo;
+      m.pad[0] = m.pad[1] = m.pad[2] = 0;
       if (bad) {
         atomicOr(&status_s, bad);
         m.len_q = 0;  // no tiles, rows untouched

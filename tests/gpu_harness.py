@@ -56,16 +56,21 @@ def run_thd(batch: wl.ThdBatch, kernel: int = bd.KERNEL_AUTO, device="cuda", gap
     offs = [ints(x) for x in row_offs]
     mask = torch.from_numpy(np.ascontiguousarray(batch.mask_type, dtype=np.int8)).to(device)
     qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
+    win = None if batch.window_left is None else ints(batch.window_left)
     plan = bd.plan_for_tensors(q, k, v, o, batch.batch, batch.cap_s, batch.stats_layout,
                                batch.softmax_scale, kernel, flags, mult)
     ws = bd.alloc_workspace(plan, device)
     for _ in range(reps):
-        bd.thd_attn_fwd(plan, q, k, v, o, stats, cu_q, cu_k, *offs, mask, qco, ws, stream)
+        if win is None:
+            bd.thd_attn_fwd(plan, q, k, v, o, stats, cu_q, cu_k, *offs, mask, qco, ws, stream)
+        else:
+            bd.thd_attn_fwd_window(plan, q, k, v, o, stats, cu_q, cu_k, *offs, mask, qco, win, ws,
+                                   stream)
     status = bd.thd_attn_read_status(plan, ws, stream)
     torch.cuda.synchronize()
     return dict(o=o.cpu(), o_backing=ob.cpu(), stats=stats.cpu(), status=status, plan=plan,
                 ws=ws, dev=dict(q=q, k=k, v=v, o=o, stats=stats, cu_q=cu_q, cu_k=cu_k, offs=offs,
-                                mask=mask, qco=qco))
+                                mask=mask, qco=qco, win=win))
 
 
 def check_parity(batch: wl.ThdBatch, res, row_subset=None, tol=None):

@@ -1,7 +1,7 @@
 """CPU mirror of the setup kernel's outputs (metadata, pair list, header words).
 
 The setup kernel's contract, restated independently: per sequence
-``(len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift)``; invalid
+``(len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift, lo_shift, 0, 0, 0)``; invalid
 sequences (negative length, offset outside capacity, unknown mask) get
 ``len_q = 0`` and a status bit; every valid sequence contributes
 ``ceil(len_q / rows_per_unit)`` pairs ``(b, row0)``, ordered by descending cost
@@ -14,6 +14,7 @@ import numpy as np
 
 COST_BINS = 1024
 COST_GROUPS = 11
+NO_LOWER_BOUND = -(1 << 30)
 
 
 def cost_group(c: int) -> int:
@@ -71,14 +72,15 @@ def split_entries(pairs, h_q: int, num_ctas: int, max_split: int, allow_split: b
 
 
 def mirror(batch, rows_per_unit: int, keys_per_tile: int, max_pairs: int, caps=None):
-    """Expected (meta [B, 8] int32, pairs list of (b, row0, cost), status, num_pairs).
-    Costs are the unclamped KV-tile counts clamped to the bucket range."""
+    """Expected (meta [B, 12] int32, pairs list of (b, row0, cost), status, num_pairs).
+    Costs are the KV-tile counts (first visible tile of the pair's first row through
+    the last of its last row) clamped to the bucket range."""
     lq = batch.lens_q()
     lk = batch.lens_k()
     if caps is None:
         caps = (batch.q.shape[0], batch.k.shape[0], batch.v.shape[0], batch.cap_o, batch.cap_s)
     cap_q, cap_k, cap_v, cap_o, cap_s = caps
-    meta = np.zeros((batch.batch, 8), dtype=np.int64)
+    meta = np.zeros((batch.batch, 12), dtype=np.int64)
     status = 0
     pairs = []
     for b in range(batch.batch):
@@ -100,8 +102,12 @@ def mirror(batch, rows_per_unit: int, keys_per_tile: int, max_pairs: int, caps=N
             shift = 0
         else:
             shift = int(lk[b] - lq[b]) if batch.q_causal_offset is None else int(batch.q_causal_offset[b])
+        lo = NO_LOWER_BOUND
+        win = None if batch.window_left is None else int(batch.window_left[b])
+        if win is not None and win >= 0 and mt in (1, 2):
+            lo = max(NO_LOWER_BOUND, min(1 << 30, shift - win))
         shift = max(-(1 << 30), min(1 << 30, shift))
-        meta[b] = [0 if bad else lq[b], lk[b], *offs, shift]
+        meta[b] = [0 if bad else lq[b], lk[b], *offs, shift, lo, 0, 0, 0]
         status |= bad
         if bad:
             continue
@@ -109,7 +115,8 @@ def mirror(batch, rows_per_unit: int, keys_per_tile: int, max_pairs: int, caps=N
             row0 = t * rows_per_unit
             r_end = min(int(lq[b]), row0 + rows_per_unit)
             kmax = min(int(lk[b]), r_end + shift)
-            cost = 0 if kmax <= 0 else (kmax + keys_per_tile - 1) // keys_per_tile
+            first = max(0, row0 + lo) // keys_per_tile
+            cost = 0 if kmax <= 0 else max(0, (kmax + keys_per_tile - 1) // keys_per_tile - first)
             pairs.append((b, row0, min(cost, COST_BINS - 1)))
     if len(pairs) > max_pairs:
         status |= TILE_OVERFLOW

@@ -133,7 +133,7 @@ def test_schedule_matches_cpu_mirror(name, kw, kernel, flags):
     assert header[16] == n_split
     starts = schedule_mirror.group_starts([(b, r, c) for b, r, _, _, c in entries])
     assert list(header[4:4 + len(starts)]) == starts
-    meta = ws[meta_off:meta_off + 32 * batch.batch].view(np.int32).reshape(batch.batch, 8)
+    meta = ws[meta_off:meta_off + 48 * batch.batch].view(np.int32).reshape(batch.batch, 12)
     assert np.array_equal(meta, meta_exp)
     recs = ws[pairs_off:pairs_off + 16 * n_exp].view(np.int32).reshape(n_exp, 4)
     # same multiset of (b, row0, half, halves); costs non-increasing along the list;
@@ -282,3 +282,75 @@ def test_element_offset_not_a_whole_row_is_flagged():
     # sequence 1's rows untouched, the others written
     o1 = o.cpu().view(torch.uint8)[int(batch.off_o[1]):int(batch.off_o[1]) + int(batch.lens_q()[1])]
     assert (o1 == wl.SENTINEL_BYTE).all()
+
+
+# ------------------------------------------------------------------ left window
+def _with_window(batch: wl.ThdBatch, windows) -> wl.ThdBatch:
+    import dataclasses
+    w = np.array([windows[i % len(windows)] for i in range(batch.batch)], dtype=np.int32)
+    return dataclasses.replace(batch, window_left=w)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("seed", range(8))
+def test_random_packs_window(seed, kernel):
+    """Per-sequence left windows on the causal masks (TransformerEngine PR #3274,
+    per-policy windows): zero, short, longer than the sequence and unbounded, over
+    random ragged packs with mixed masks and causal offsets."""
+    rng = np.random.default_rng(3000 + seed)
+    dtype = ["bf16", "fp16"][seed % 2]
+    d = [64, 128][(seed // 2) % 2]
+    h_kv = int(rng.integers(1, 3))
+    h_q = h_kv * int(rng.integers(1, 3))
+    batch = wl.random_pack(4000 + seed, batch=int(rng.integers(1, 7)), max_len=int(rng.integers(1, 900)),
+                           h_q=h_q, h_kv=h_kv, d=d, dtype=dtype, with_window=True)
+    res = run_thd(batch, kernel=kernel)
+    assert res["status"] == 0
+    check_parity(batch, res)
+    check_untouched(batch, res)
+
+
+@pytest.mark.parametrize("windows", [(0,), (1, 127, 128, 129), (300, 700), (-1, 5000)])
+def test_window_split_matches_unsplit(windows):
+    """Window ranges through the KV split (halves of the pair's tile span) agree
+    with the unsplit path and with the oracle."""
+    batch = _with_window(wl.make("cp_chunks", **SMALL["cp_chunks"]), windows)
+    a = run_thd(batch)
+    b = run_thd(batch, flags=bd.FLAG_NO_KV_SPLIT)
+    assert a["status"] == 0 and b["status"] == 0
+    check_parity(batch, a)
+    check_parity(batch, b)
+    check_untouched(batch, a)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_window_long_sequences(kernel):
+    """Windows far shorter than the sequence: most KV tiles of each unit are
+    skipped, and the two query sub-tiles of a unit start on different tiles."""
+    batch = _with_window(wl.padded_causal(b=3, h=2, min_len=2500, max_len=3000), (256, 1000, 70))
+    res = run_thd(batch, kernel=kernel)
+    assert res["status"] == 0
+    check_parity(batch, res)
+    check_untouched(batch, res)
+
+
+def test_window_schedule_matches_cpu_mirror():
+    """With a window the pair cost is the span from the first row's lowest visible
+    tile to the last row's highest; setup metadata and order match the CPU mirror."""
+    batch = _with_window(wl.make("cp_chunks", docs=2, k_len=2048, q_len=768, h=4), (200, -1, 600, 0))
+    res = run_thd(batch)
+    plan = res["plan"]
+    ws = res["ws"].cpu().numpy()
+    hdr, meta_off, base_off, pairs_off = plan.workspace_layout
+    header = ws[hdr:hdr + 128].view(np.uint32)
+    meta_exp, pairs_exp, status_exp, _ = schedule_mirror.mirror(
+        batch, plan.rows_per_unit, plan.keys_per_tile, plan.max_pairs)
+    meta = ws[meta_off:meta_off + 48 * batch.batch].view(np.int32).reshape(batch.batch, 12)
+    assert np.array_equal(meta, meta_exp)
+    num_ctas = min(torch.cuda.get_device_properties(0).multi_processor_count, 2 * plan.max_pairs * batch.h_q)
+    max_split = min(plan.max_pairs, -(-4 * 160 // batch.h_q))
+    entries, n_split = schedule_mirror.split_entries(pairs_exp, batch.h_q, num_ctas, max_split, True)
+    assert header[1] == status_exp and header[2] == len(entries) and header[16] == n_split
+    starts = schedule_mirror.group_starts([(b, r, c) for b, r, _, _, c in entries])
+    assert list(header[4:4 + len(starts)]) == starts
+    check_parity(batch, res)
