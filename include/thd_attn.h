@@ -1,5 +1,6 @@
 /*
- * thd_attn.h -- C ABI of the GB300 (sm_103a) packed-THD forward attention library.
+ * thd_attn.h -- C ABI of the GB300 (sm_103a) packed-THD attention library
+ * (forward, and its backward at the end of this file).
  *
  * Operation (scaled-dot-product attention forward with log-sum-exp Stats over a
  * packed, ragged "THD" batch):
@@ -251,6 +252,59 @@ thd_status_t thd_attn_fwd_static_ws(thd_attn_plan_t plan, const void* q, const v
 
 /* Capacity in bytes of the static scratch array used by thd_attn_fwd_static_ws. */
 size_t thd_attn_static_workspace_capacity(void);
+
+/* ------------------------------------------------------------------ backward
+ *
+ * Gradients of the forward pass above (ragged SDPA backward over the same
+ * metadata and Stats layouts: NVIDIA/cudnn-frontend PR #462, sections "What" and
+ * "Root cause", which name the backward's per-row softmax sums and dQ/dK/dV
+ * intermediates in THD layout). For an upstream gradient dO (the loss is
+ * L = sum_i <O_i, dO_i>), per sequence b and query head h (kv head g):
+ *
+ *     P_ij  = exp(s_ij - LSE_i) on visible keys, 0 elsewhere (LSE_i read from Stats)
+ *     D_i   = <dO_i, O_i>                               (O read from the O view)
+ *     dV_j  = sum_i P_ij dO_i
+ *     dS_ij = P_ij (<dO_i, v_j> - D_i)
+ *     dQ_i  = softmax_scale * sum_j dS_ij k_j
+ *     dK_j  = softmax_scale * sum_i dS_ij q_i
+ *
+ *   dK and dV of kv head g sum over the query heads of its group. dQ rows are
+ *   written at off_q[b] + i, dK rows at off_k[b] + j, dV rows at off_v[b] + j
+ *   (each gradient shares its primal tensor's row offsets); dO is read at
+ *   off_o[b] + i. A query row with no visible key gets dQ = 0; a key no query
+ *   sees gets dK = dV = 0. Rows outside the sequences are never written.
+ *   Masks, causal offsets and windows as in thd_attn_fwd_window.
+ */
+typedef struct {
+  thd_attn_desc_t fwd;            /* the forward's Q, K, V, O views, Stats, scale, kernel, flags */
+  int64_t cap_rows[4];            /* index 0..3: dO, dQ, dK, dV views (same dtype as the forward); */
+  int64_t stride_tok[4];          /*   each gradient view needs at least its primal view's rows */
+  int64_t stride_head[4];
+  int64_t bytes[4];               /* 0 = not checked */
+} thd_attn_bwd_desc_t;
+
+/* Validate a backward descriptor and pick the kernels (host only). The plan is
+ * used with thd_attn_bwd (not thd_attn_fwd); *workspace_bytes as for thd_attn_plan.
+ * THD_FLAG_ELEMENT_OFFSETS and THD_FLAG_NO_KV_SPLIT are accepted; element offsets
+ * of dO / dQ / dK / dV follow their primal tensors' token strides. */
+thd_status_t thd_attn_plan_bwd(thd_attn_plan_t* out, const thd_attn_bwd_desc_t* desc,
+                               size_t* workspace_bytes);
+
+/* Enqueue the backward pass on `stream`.
+ *   q, k, v, o, stats  the forward's inputs, output and LSE (read only)
+ *   d_o                upstream gradient, dO view of the plan (read only)
+ *   dq, dk, dv         gradient views of the plan (written rows only)
+ *   remaining metadata as in thd_attn_fwd_window (window_left may be NULL)
+ * Asynchronous, no allocation, no device->host read; device data errors surface
+ * through thd_attn_read_status. Gradient rows of different sequences that overlap
+ * race. */
+thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, const void* v,
+                          const void* o, const void* d_o, const float* stats, void* dq, void* dk,
+                          void* dv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                          const int32_t* off_q, const int32_t* off_k, const int32_t* off_v,
+                          const int32_t* off_o, const int32_t* off_s, const int8_t* mask_type,
+                          const int32_t* q_causal_offset, const int32_t* window_left,
+                          void* workspace, void* stream);
 
 #ifdef __cplusplus
 }

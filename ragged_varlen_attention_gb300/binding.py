@@ -52,12 +52,22 @@ class ThdAttnDesc(ctypes.Structure):
     ]
 
 
+class ThdAttnBwdDesc(ctypes.Structure):
+    _fields_ = [
+        ("fwd", ThdAttnDesc),
+        ("cap_rows", ctypes.c_int64 * 4),      # dO, dQ, dK, dV
+        ("stride_tok", ctypes.c_int64 * 4),
+        ("stride_head", ctypes.c_int64 * 4),
+        ("bytes", ctypes.c_int64 * 4),
+    ]
+
+
 _LIB = None
 _EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_plan_kernel",
             "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
             "thd_attn_status_string", "thd_attn_view_span_bytes", "thd_attn_profile_enable",
             "thd_attn_profile_read", "thd_attn_fwd_static_ws", "thd_attn_static_workspace_capacity",
-            "thd_attn_fwd_window"]
+            "thd_attn_fwd_window", "thd_attn_plan_bwd", "thd_attn_bwd"]
 
 
 def library_path() -> str:
@@ -81,6 +91,11 @@ def load_library():
     lib.thd_attn_fwd.restype = ctypes.c_int
     lib.thd_attn_fwd_window.argtypes = [vp] * 18
     lib.thd_attn_fwd_window.restype = ctypes.c_int
+    lib.thd_attn_plan_bwd.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(ThdAttnBwdDesc),
+                                      ctypes.POINTER(ctypes.c_size_t)]
+    lib.thd_attn_plan_bwd.restype = ctypes.c_int
+    lib.thd_attn_bwd.argtypes = [vp] * 22
+    lib.thd_attn_bwd.restype = ctypes.c_int
     lib.thd_attn_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.thd_attn_read_status.restype = ctypes.c_int
     lib.thd_attn_plan_kernel.argtypes = [vp]
@@ -178,6 +193,33 @@ def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: 
     return thd_attn_plan(desc)
 
 
+def plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch: int, cap_rows_stats: int,
+                         stats_layout: int, softmax_scale=None, kernel: int = KERNEL_AUTO,
+                         flags: int = 0, offset_multiplier: int = 0) -> ThdAttnPlan:
+    """Backward plan from [rows, heads, d] views of the forward's tensors and of the
+    gradients dO, dQ, dK, dV (see ``thd_attn_plan_bwd`` in include/thd_attn.h)."""
+    for t in (q, k, v, o, d_o, dq, dk, dv):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("tensors must be [rows, heads, d] views with a contiguous last dim")
+    bd = ThdAttnBwdDesc()
+    bd.fwd = make_desc(q.dtype, batch, q.shape[1], k.shape[1], q.shape[2],
+                       [t.shape[0] for t in (q, k, v, o)], [t.stride(0) for t in (q, k, v, o)],
+                       [t.stride(1) for t in (q, k, v, o)], [_view_bytes(t) for t in (q, k, v, o)],
+                       cap_rows_stats, stats_layout, softmax_scale, kernel, flags, offset_multiplier)
+    for i, t in enumerate((d_o, dq, dk, dv)):
+        bd.cap_rows[i] = t.shape[0]
+        bd.stride_tok[i] = t.stride(0)
+        bd.stride_head[i] = t.stride(1)
+        bd.bytes[i] = _view_bytes(t)
+    lib = load_library()
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.thd_attn_plan_bwd(ctypes.byref(handle), ctypes.byref(bd), ctypes.byref(ws))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_plan_bwd")
+    return ThdAttnPlan(handle.value, ws.value, bd.fwd)
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -214,6 +256,20 @@ def thd_attn_fwd_window(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_s
                                  _stream_handle(stream))
     if st != 0:
         raise ThdAttnError(st, "thd_attn_fwd_window")
+
+
+def thd_attn_bwd(plan: ThdAttnPlan, q, k, v, o, d_o, stats, dq, dk, dv, cu_seqlens_q,
+                 cu_seqlens_kv, off_q, off_k, off_v, off_o, off_s, mask_type, q_causal_offset,
+                 window_left, workspace, stream=None) -> None:
+    """Enqueue the backward pass (see ``thd_attn_bwd`` in include/thd_attn.h)."""
+    lib = load_library()
+    st = lib.thd_attn_bwd(ctypes.c_void_p(plan.handle), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o),
+                          _ptr(stats), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q),
+                          _ptr(cu_seqlens_kv), _ptr(off_q), _ptr(off_k), _ptr(off_v), _ptr(off_o),
+                          _ptr(off_s), _ptr(mask_type), _ptr(q_causal_offset), _ptr(window_left),
+                          _ptr(workspace), _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_bwd")
 
 
 def thd_attn_fwd_static_ws(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q,

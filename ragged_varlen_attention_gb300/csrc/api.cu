@@ -248,7 +248,7 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
                                  const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
                                  const int32_t* off_s, const int8_t* mask, const int32_t* qco,
                                  const int32_t* window_left, void* workspace, void* stream_ptr) {
-  if (!plan) return THD_ERR_INVALID_ARG;
+  if (!plan || plan->is_bwd) return THD_ERR_INVALID_ARG;
   const thd_attn_desc_t& d = plan->desc;
   if (!workspace) return THD_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return THD_ERR_WORKSPACE;
@@ -274,6 +274,8 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
   sp.keys_per_tile = plan->keys_per_tile;
   sp.max_pairs = plan->max_pairs;
   sp.h_q = d.h_q;
+  sp.key_axis = 0;
+  sp.unit_heads = d.h_q;
   sp.allow_split = plan->allow_split;
   sp.element_offsets = (d.flags & THD_FLAG_ELEMENT_OFFSETS) ? 1 : 0;
   sp.offset_multiplier = d.offset_multiplier > 0 ? d.offset_multiplier : 1;
@@ -351,9 +353,197 @@ thd_status_t thd_attn_read_status(thd_attn_plan_t plan, const void* workspace, u
   if (!workspace) return THD_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const char* src = static_cast<const char*>(workspace) + plan->ws_off[0] + 4 * thd::kHdrStatus;
-  if (cudaMemcpyAsync(host_out, src, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  uint32_t words[2] = {0u, 0u};
+  if (cudaMemcpyAsync(&words[0], src, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return THD_ERR_CUDA;
+  if (plan->is_bwd) {
+    // the key-axis schedule of the backward keeps its own status word
+    const char* src_k = static_cast<const char*>(workspace) + plan->ws_off_b[0] + 4 * thd::kHdrStatus;
+    if (cudaMemcpyAsync(&words[1], src_k, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return THD_ERR_CUDA;
+  }
   if (cudaStreamSynchronize(stream) != cudaSuccess) return THD_ERR_CUDA;
+  *host_out = words[0] | words[1];
+  return THD_OK;
+}
+
+// ------------------------------------------------------------------------- backward
+
+thd_status_t thd_attn_plan_bwd(thd_attn_plan_t* out, const thd_attn_bwd_desc_t* desc, size_t* ws_bytes) {
+  if (!out || !desc || !ws_bytes) return THD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const thd_attn_desc_t& d = desc->fwd;
+  // the forward descriptor's own checks (views, capacities, scale, kernel request)
+  thd_attn_plan_t fp = nullptr;
+  size_t fws = 0;
+  const thd_status_t st = thd_attn_plan(&fp, &d, &fws);
+  if (st != THD_OK) return st;
+  thd_attn_plan_destroy(fp);
+  // gradient views: same dtype; each at least as many rows as its primal view
+  // (dO <-> O, dQ <-> Q, dK <-> K, dV <-> V), and its all-axes span inside its bytes
+  const int eb = elem_bytes(d.dtype);
+  const int64_t prim_rows[4] = {d.cap_rows[3], d.cap_rows[0], d.cap_rows[1], d.cap_rows[2]};
+  const int64_t heads[4] = {d.h_q, d.h_q, d.h_kv, d.h_kv};
+  for (int i = 0; i < 4; ++i) {
+    if (desc->cap_rows[i] < prim_rows[i] || desc->cap_rows[i] >= (int64_t(1) << 31)) return THD_ERR_INVALID_ARG;
+    if (desc->stride_tok[i] < 0 || desc->stride_head[i] < 0 || desc->bytes[i] < 0) return THD_ERR_INVALID_ARG;
+    if (desc->bytes[i] == 0) continue;
+    const int64_t span = thd_attn_view_span_bytes(desc->cap_rows[i], heads[i], d.d, desc->stride_tok[i],
+                                                  desc->stride_head[i], eb);
+    if (span > desc->bytes[i]) return THD_ERR_CAPACITY;
+  }
+  if (d.kernel == THD_KERNEL_TCGEN05) return THD_ERR_UNSUPPORTED;
+
+  auto* p = new (std::nothrow) thd_attn_plan_s;
+  if (!p) return THD_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->desc = d;
+  p->is_bwd = 1;
+  p->kernel = THD_KERNEL_SIMT;
+  float scale = d.softmax_scale;
+  if (std::isnan(scale)) scale = 1.0f / std::sqrt((float)d.d);
+  p->scale = scale;
+  p->elem_bytes = eb;
+  for (int i = 0; i < 4; ++i) {
+    p->g_cap_rows[i] = desc->cap_rows[i];
+    p->g_stride_tok[i] = desc->stride_tok[i];
+    p->g_stride_head[i] = desc->stride_head[i];
+  }
+  p->rows_per_unit = thd::kBwdRowsPerUnit;
+  p->keys_per_tile = thd::kBwdKeysPerUnit;
+  if (d.stats_layout == THD_STATS_TOKEN_MAJOR) {
+    p->stats_tok = d.h_q;
+    p->stats_head = 1;
+  } else {
+    p->stats_tok = 1;
+    p->stats_head = d.cap_rows_stats;
+  }
+  // non-overlapping Q rows bound the query-axis pairs, non-overlapping K rows the key-axis ones
+  const int64_t max_q = (int64_t)d.batch + (d.cap_rows[0] + p->rows_per_unit - 1) / p->rows_per_unit + 1;
+  const int64_t max_k = (int64_t)d.batch + (d.cap_rows[1] + thd::kBwdKeysPerUnit - 1) / thd::kBwdKeysPerUnit + 1;
+  if (max_q * d.h_q >= (int64_t(1) << 31) || max_k * d.h_kv >= (int64_t(1) << 31)) {
+    delete p;
+    return THD_ERR_UNSUPPORTED;
+  }
+  p->max_pairs = (int32_t)max_q;
+  p->max_pairs_k = (int32_t)max_k;
+  p->allow_split = 0;
+  p->max_split = 0;
+  int64_t off = 0;
+  p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
+  p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
+  p->ws_off[2] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
+  p->ws_off[3] = off; off = align_up(off + max_q * (int64_t)sizeof(thd::PairRec), kAlign);
+  p->ws_off[4] = p->ws_off[5] = p->ws_off[6] = off;
+  p->ws_off_b[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
+  p->ws_off_b[1] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
+  p->ws_off_b[2] = off; off = align_up(off + max_k * (int64_t)sizeof(thd::PairRec), kAlign);
+  p->ws_off_b[3] = off; off = align_up(off + (int64_t)d.h_q * d.cap_rows[0] * 8, kAlign);
+  p->ws_bytes = (size_t)off;
+  *ws_bytes = p->ws_bytes;
+  *out = p;
+  return THD_OK;
+}
+
+thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, const void* v, const void* o,
+                          const void* d_o, const float* stats, void* dq, void* dk, void* dv, const int32_t* cu_q,
+                          const int32_t* cu_k, const int32_t* off_q, const int32_t* off_k, const int32_t* off_v,
+                          const int32_t* off_o, const int32_t* off_s, const int8_t* mask, const int32_t* qco,
+                          const int32_t* window_left, void* workspace, void* stream_ptr) {
+  if (!plan || !plan->is_bwd) return THD_ERR_INVALID_ARG;
+  const thd_attn_desc_t& d = plan->desc;
+  if (!workspace) return THD_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return THD_ERR_WORKSPACE;
+  if (d.batch > 0 && (!cu_q || !cu_k || !off_q || !off_k || !off_v || !off_o || !off_s || !mask))
+    return THD_ERR_INVALID_ARG;
+  const void* prim[4] = {q, k, v, o};
+  for (int i = 0; i < 4; ++i)
+    if (!prim[i] && d.cap_rows[i] > 0) return THD_ERR_INVALID_ARG;
+  const void* grads[4] = {d_o, dq, dk, dv};
+  for (int i = 0; i < 4; ++i)
+    if (!grads[i] && plan->g_cap_rows[i] > 0) return THD_ERR_INVALID_ARG;
+  if (!stats && d.cap_rows_stats > 0) return THD_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  const int num_sms = num_sms_of_current_device();
+  if (num_sms <= 0) return THD_ERR_CUDA;
+
+  thd::SetupParams sp;
+  sp.cu_q = cu_q; sp.cu_k = cu_k;
+  sp.off_q = off_q; sp.off_k = off_k; sp.off_v = off_v; sp.off_o = off_o; sp.off_s = off_s;
+  sp.mask = mask; sp.qco = qco; sp.window = window_left;
+  sp.cap_q = d.cap_rows[0]; sp.cap_k = d.cap_rows[1]; sp.cap_v = d.cap_rows[2]; sp.cap_o = d.cap_rows[3];
+  sp.cap_s = d.cap_rows_stats;
+  sp.batch = d.batch;
+  sp.h_q = d.h_q;
+  sp.allow_split = 0;
+  sp.element_offsets = (d.flags & THD_FLAG_ELEMENT_OFFSETS) ? 1 : 0;
+  sp.offset_multiplier = d.offset_multiplier > 0 ? d.offset_multiplier : 1;
+  for (int i = 0; i < 4; ++i) sp.tok_stride[i] = d.stride_tok[i] > 0 ? d.stride_tok[i] : 1;
+  sp.tok_stride[4] = plan->stats_tok > 0 ? plan->stats_tok : 1;
+  sp.max_split = 0;
+  sp.num_ctas = num_sms;
+  sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
+  sp.splits = nullptr;
+  // query axis: dQ units of rows_per_unit rows, cost in KV tiles
+  sp.key_axis = 0;
+  sp.unit_heads = d.h_q;
+  sp.rows_per_unit = plan->rows_per_unit;
+  sp.keys_per_tile = thd::kBwdKeysPerUnit;
+  sp.max_pairs = plan->max_pairs;
+  sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
+  sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
+  sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
+  if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
+  thd::BwdParams bp;
+  bp.header_q = sp.header;
+  bp.counter_q = sp.header + thd::kHdrCounter;
+  bp.pairs_q = sp.pairs;
+  // key axis: dK/dV units of kBwdKeysPerUnit keys, cost in query tiles
+  sp.key_axis = 1;
+  sp.unit_heads = d.h_kv;
+  sp.rows_per_unit = thd::kBwdKeysPerUnit;
+  sp.keys_per_tile = plan->rows_per_unit;
+  sp.max_pairs = plan->max_pairs_k;
+  sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off_b[0]);
+  sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off_b[1]);
+  sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off_b[2]);
+  if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
+  bp.header_k = sp.header;
+  bp.counter_k = sp.header + thd::kHdrCounter;
+  bp.pairs_k = sp.pairs;
+
+  bp.q = q; bp.k = k; bp.v = v; bp.o = o; bp.d_o = d_o; bp.stats = stats;
+  bp.dq = dq; bp.dk = dk; bp.dv = dv;
+  for (int i = 0; i < 4; ++i) {
+    bp.stride_tok[i] = d.stride_tok[i];
+    bp.stride_head[i] = d.stride_head[i];
+    bp.stride_tok[4 + i] = plan->g_stride_tok[i];
+    bp.stride_head[4 + i] = plan->g_stride_head[i];
+  }
+  bp.stats_tok = plan->stats_tok;
+  bp.stats_head = plan->stats_head;
+  bp.h_q = d.h_q; bp.h_kv = d.h_kv; bp.d = d.d;
+  bp.scale = plan->scale;
+  bp.scale_log2 = plan->scale * 1.4426950408889634f;
+  bp.status = const_cast<uint32_t*>(bp.header_q) + thd::kHdrStatus;
+  bp.meta = sp.meta;
+  bp.ld = reinterpret_cast<float2*>(ws + plan->ws_off_b[3]);
+  bp.ld_rows = d.cap_rows[0];
+  bp.rows_per_unit = plan->rows_per_unit;
+  bp.keys_per_unit = thd::kBwdKeysPerUnit;
+  bp.has_window = window_left != nullptr ? 1 : 0;
+
+  if (thd::launch_bwd_prep(bp, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
+  const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
+  if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
+    return THD_ERR_CUDA;
+  if (thd::launch_bwd_simt(bp, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
+  if (prof) {
+    if (cudaEventRecord(plan->prof_events[2 * plan->prof_count + 1], stream) != cudaSuccess)
+      return THD_ERR_CUDA;
+    ++plan->prof_count;
+  }
   return THD_OK;
 }
 

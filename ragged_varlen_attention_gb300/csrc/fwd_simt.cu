@@ -15,6 +15,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "convert.cuh"
 #include "internal.h"
 
 namespace thd {
@@ -24,16 +25,6 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kBN = kSimtKeysPerTile;
 constexpr int kDPT = 64;  // head-dim elements per thread
-
-template <typename T> __device__ __forceinline__ float to_f32(T x);
-template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
-template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
-
-template <typename T> __device__ __forceinline__ T from_f32(float x);
-template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
-template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
-template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 
 template <typename T, int TPR>
 __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdParams p, int rows_per_unit) {

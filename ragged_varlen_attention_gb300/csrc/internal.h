@@ -73,10 +73,12 @@ struct SetupParams {
   const int32_t* window;    // may be null
   int64_t cap_q, cap_k, cap_v, cap_o, cap_s;
   int32_t batch;
-  int32_t rows_per_unit;
-  int32_t keys_per_tile;
+  int32_t rows_per_unit;    // rows (keys on the key axis) of one scheduled unit
+  int32_t keys_per_tile;    // keys per KV tile (query rows per tile on the key axis)
   int32_t max_pairs;        // pairs before splitting
   int32_t h_q;
+  int32_t key_axis;         // 0: units over query rows (cost = KV tiles); 1: over keys (cost = query tiles)
+  int32_t unit_heads;       // heads each pair is scheduled for (h_q, or h_kv on the key axis)
   int32_t allow_split;      // KV split permitted (workspace holds the partial buffers)
   int32_t element_offsets;  // offsets are elements (x multiplier): divide by the token strides
   int64_t offset_multiplier;
@@ -134,6 +136,41 @@ __device__ __forceinline__ void work_to_unit(const uint32_t* header, uint32_t w,
   head = (int)(kvh * grp + rem % grp);
 }
 
+// Arguments of the backward kernels. Tensor index of the stride arrays:
+// 0 Q, 1 K, 2 V, 3 O, 4 dO, 5 dQ, 6 dK, 7 dV.
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* d_o;
+  const float* stats;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t stride_tok[8];
+  int64_t stride_head[8];
+  int64_t stats_tok, stats_head;
+  int32_t h_q, h_kv, d;
+  float scale;              // softmax_scale
+  float scale_log2;         // softmax_scale * log2(e)
+  // query-axis schedule (dQ units: rows_per_unit query rows x one query head)
+  const uint32_t* header_q;
+  uint32_t* counter_q;
+  const PairRec* pairs_q;
+  // key-axis schedule (dK/dV units: keys_per_unit keys x one kv head)
+  const uint32_t* header_k;
+  uint32_t* counter_k;
+  const PairRec* pairs_k;
+  uint32_t* status;
+  const SeqMeta* meta;
+  float2* ld;               // [h_q][ld_rows]: (LSE * log2(e), D = <dO, O>) per query row
+  int64_t ld_rows;          // rows of Q's view: ld index = h * ld_rows + off_q + i
+  int32_t rows_per_unit;
+  int32_t keys_per_unit;
+  int32_t has_window;
+};
+
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
@@ -144,6 +181,11 @@ cudaError_t launch_fwd_simt(const FwdParams& p, thd_dtype_t dtype, int rows_per_
 int simt_rows_per_unit(int d);
 cudaError_t launch_combine(const FwdParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
 constexpr int kSimtKeysPerTile = 32;
+// backward: preprocess (LSE and D per query row), then the dQ and dK/dV kernels
+constexpr int kBwdRowsPerUnit = 128;   // query rows of a dQ unit
+constexpr int kBwdKeysPerUnit = 128;   // keys of a dK/dV unit
+cudaError_t launch_bwd_prep(const BwdParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd_simt(const BwdParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
 
 }  // namespace thd
 
@@ -160,6 +202,13 @@ struct thd_attn_plan_s {
   int64_t ws_off[7];        // header, meta, pair_base, pairs, splits, part_o, part_lse
   int32_t allow_split;
   int32_t max_split;
+  // backward plans (thd_attn_plan_bwd)
+  int32_t is_bwd;
+  int64_t g_cap_rows[4];    // dO, dQ, dK, dV
+  int64_t g_stride_tok[4];
+  int64_t g_stride_head[4];
+  int32_t max_pairs_k;      // key-axis pair capacity
+  int64_t ws_off_b[4];      // key-axis header, pair_base, pairs; (LSE, D) rows
   // optional attention-kernel timing (thd_attn_profile_enable)
   int32_t prof_slots;
   int32_t prof_count;

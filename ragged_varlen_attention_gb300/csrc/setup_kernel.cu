@@ -50,14 +50,32 @@ __device__ __forceinline__ int32_t block_inclusive_scan(int32_t x, int32_t* warp
 
 // number of KV tiles the pair starting at row0 must visit: from the tile of the
 // first row's lowest visible key to the tile of the last row's highest
-__device__ __forceinline__ int32_t pair_cost(const SeqMeta& m, int32_t row0, int32_t rows_per_unit,
-                                             int32_t keys_per_tile) {
+__device__ __forceinline__ int32_t query_pair_cost(const SeqMeta& m, int32_t row0, int32_t rows_per_unit,
+                                                   int32_t keys_per_tile) {
   const int64_t r_end = min64((int64_t)m.len_q, (int64_t)row0 + rows_per_unit);
   const int64_t kmax = min64((int64_t)m.len_k, r_end + (int64_t)m.shift);
   if (kmax <= 0) return 0;
   const int64_t kmin = max64(0, (int64_t)row0 + (int64_t)m.lo_shift);
   const int64_t first = kmin / keys_per_tile, end = (kmax + keys_per_tile - 1) / keys_per_tile;
   return (int32_t)max64(0, end - first);
+}
+
+// key axis (backward dK/dV units): number of query tiles of `rows_per_tile` rows
+// that see any key of [k0, k0 + keys_per_unit): key j is seen by rows
+// j - shift <= i <= j - lo_shift
+__device__ __forceinline__ int32_t key_pair_cost(const SeqMeta& m, int32_t k0, int32_t keys_per_unit,
+                                                 int32_t rows_per_tile) {
+  const int64_t k_end = min64((int64_t)m.len_k, (int64_t)k0 + keys_per_unit);
+  if (k_end <= k0) return 0;
+  const int64_t i_lo = max64(0, (int64_t)k0 - (int64_t)m.shift);
+  const int64_t i_hi = min64((int64_t)m.len_q, (k_end - 1) - (int64_t)m.lo_shift + 1);
+  if (i_hi <= i_lo) return 0;
+  return (int32_t)((i_hi + rows_per_tile - 1) / rows_per_tile - i_lo / rows_per_tile);
+}
+
+__device__ __forceinline__ int32_t pair_cost(const SetupParams& p, const SeqMeta& m, int32_t row0) {
+  return p.key_axis ? key_pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile)
+                    : query_pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile);
 }
 
 // group of a (clamped) cost: 0 for 512..1023, 1 for 256..511, ..., 9 for 1, 10 for 0
@@ -140,7 +158,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
         atomicOr(&status_s, bad);
         m.len_q = 0;  // no tiles, rows untouched
       } else {
-        n = (lq + p.rows_per_unit - 1) / p.rows_per_unit;
+        n = ((p.key_axis ? lk : lq) + p.rows_per_unit - 1) / p.rows_per_unit;
       }
       p.meta[b] = m;
     }
@@ -163,12 +181,12 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    if (pair_cost(p.meta[b], row0, p.rows_per_unit, p.keys_per_tile) >= kMinSplitCost) atomicAdd(&n_splittable, 1u);
+    if (pair_cost(p, p.meta[b], row0) >= kMinSplitCost) atomicAdd(&n_splittable, 1u);
   }
   __syncthreads();
   if (tid == 0) {
     split_on = p.allow_split && total > 0 &&
-               (int64_t)total * p.h_q < (int64_t)kSplitWaves * p.num_ctas && n_splittable > 0 &&
+               (int64_t)total * p.unit_heads < (int64_t)kSplitWaves * p.num_ctas && n_splittable > 0 &&
                (int32_t)n_splittable <= p.max_split;
     n_split_done = 0;
   }
@@ -178,7 +196,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    const int32_t cost = pair_cost(p.meta[b], row0, p.rows_per_unit, p.keys_per_tile);
+    const int32_t cost = pair_cost(p, p.meta[b], row0);
     if (split_on && cost >= kMinSplitCost) {
       const int32_t c0 = min(cost / 2, kCostBins - 1), c1 = min(cost - cost / 2, kCostBins - 1);
       atomicAdd(&hist[c0], 1u);
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    const int32_t cost = pair_cost(p.meta[b], row0, p.rows_per_unit, p.keys_per_tile);
+    const int32_t cost = pair_cost(p, p.meta[b], row0);
     if (split_on && cost >= kMinSplitCost) {
       const int32_t part = (int32_t)atomicAdd(&n_split_done, 1u);
       SplitRec sr;
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
     p.header[kHdrCounter] = 0u;
     p.header[kHdrStatus] = status_s;
     p.header[kHdrNumPairs] = acc;
-    p.header[kHdrNumTiles] = acc * (uint32_t)p.h_q;
+    p.header[kHdrNumTiles] = acc * (uint32_t)p.unit_heads;
     p.header[kHdrNumSplit] = split_on ? n_splittable : 0u;
   }
 }

@@ -1,0 +1,182 @@
+"""GPU parity of the backward pass (dQ, dK, dV) against the CPU backward oracle.
+
+Inputs: the forward's O and Stats come from the forward ORACLE (cast to the
+storage types), dO is seeded N(0, 1) with NaN in pad rows, and every gradient
+buffer starts as a byte sentinel so untouched rows are checked bit for bit.
+
+Tolerance (normalised max error, |gpu - ref|_inf / max(1, |ref|_inf) per
+gradient): bf16/fp16 2e-2 -- the gradients are stored in a 16-bit type (2^-9 /
+2^-11 relative) and D_i = <dO_i, O_i> is formed from a 16-bit O, which shifts dS
+by P_ij * |dO_i| * |O_i| * 2^-9 at most; fp32 1e-4 (fp32 arithmetic throughout).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.backward as ob
+from ragged_varlen_attention_gb300 import binding as bd
+from ragged_varlen_attention_gb300 import workloads as wl
+from tests.gpu_harness import _strided
+from tests.helpers import as_f64, oracle_on_batch
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [bd.KERNEL_AUTO, bd.KERNEL_SIMT]
+TOL = {"bf16": 2e-2, "fp16": 2e-2, "fp32": 1e-4}
+SENTINEL = wl.SENTINEL_BYTE
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from ragged_varlen_attention_gb300 import build
+    build.build()
+    bd.load_library()
+
+
+def _dout(batch: wl.ThdBatch, seed: int) -> torch.Tensor:
+    g = torch.Generator().manual_seed(seed)
+    t = torch.randn((batch.cap_o, batch.h_q, batch.d), generator=g, dtype=torch.float32)
+    lq = batch.lens_q()
+    keep = np.zeros(batch.cap_o, dtype=bool)
+    for b in range(batch.batch):
+        keep[batch.off_o[b]:batch.off_o[b] + lq[b]] = True
+    t[torch.from_numpy(~keep)] = float("nan")
+    return t.to(batch.torch_dtype)
+
+
+def run_bwd(batch: wl.ThdBatch, kernel=bd.KERNEL_AUTO, gaps=(0,) * 8, seed=0, flags=0, device="cuda",
+            device_mask=None):
+    """Forward outputs from the oracle, then the backward through the C ABI
+    (``device_mask`` replaces the mask array passed to the device)."""
+    o_ref, s_ref, written = oracle_on_batch(batch)
+    o_host = batch.o_init().clone()
+    o_host[torch.from_numpy(written)] = torch.from_numpy(o_ref[written]).to(batch.torch_dtype)
+    stats_host = torch.from_numpy(s_ref.astype(np.float32))
+    d_o_host = _dout(batch, seed)
+    q, _ = _strided(batch.q, gaps[0] * batch.h_q, device)
+    k, _ = _strided(batch.k, gaps[1] * batch.h_kv, device)
+    v, _ = _strided(batch.v, gaps[2] * batch.h_kv, device)
+    o, _ = _strided(o_host, gaps[3] * batch.h_q, device)
+    d_o, _ = _strided(d_o_host, gaps[4] * batch.h_q, device)
+    grads = []
+    for src, gap, h in ((batch.q, gaps[5], batch.h_q), (batch.k, gaps[6], batch.h_kv), (batch.v, gaps[7], batch.h_kv)):
+        view, backing = _strided(torch.zeros_like(src), gap * h, device)
+        backing.view(torch.uint8).fill_(SENTINEL)
+        grads.append((view, backing))
+    (dq, dqb), (dk, dkb), (dv, dvb) = grads
+    stats = stats_host.to(device)
+    ints = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    offs = [ints(x) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)]
+    mask = torch.from_numpy(np.ascontiguousarray(batch.mask_type if device_mask is None else device_mask,
+                                                 dtype=np.int8)).to(device)
+    qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
+    win = None if batch.window_left is None else ints(batch.window_left)
+    plan = bd.plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch.batch, batch.cap_s, batch.stats_layout,
+                                   batch.softmax_scale, kernel, flags)
+    ws = bd.alloc_workspace(plan, device)
+    bd.thd_attn_bwd(plan, q, k, v, o, d_o, stats, dq, dk, dv, ints(batch.cu_seqlens_q),
+                    ints(batch.cu_seqlens_kv), *offs, mask, qco, win, ws)
+    status = bd.thd_attn_read_status(plan, ws)
+    torch.cuda.synchronize()
+    return dict(dq=dq.cpu(), dk=dk.cpu(), dv=dv.cpu(), dqb=dqb.cpu(), dkb=dkb.cpu(), dvb=dvb.cpu(),
+                status=status, plan=plan, o=o_host, d_o=d_o_host)
+
+
+def oracle_bwd(batch: wl.ThdBatch, res):
+    z = lambda t: np.zeros(tuple(t.shape))
+    return ob.thd_attention_bwd(as_f64(batch.q), as_f64(batch.k), as_f64(batch.v), as_f64(res["d_o"]),
+                                batch.cu_seqlens_q, batch.cu_seqlens_kv, batch.off_q, batch.off_k,
+                                batch.off_v, batch.off_o, batch.mask_type, batch.q_causal_offset,
+                                z(batch.q), z(batch.k), z(batch.v), softmax_scale=batch.softmax_scale,
+                                window_left=batch.window_left)
+
+
+def check_bwd(batch: wl.ThdBatch, res):
+    dq_r, dk_r, dv_r, wq, wk, wv = oracle_bwd(batch, res)
+    tol = TOL[batch.dtype]
+    errs = {}
+    for name, got, ref, w in (("dq", res["dq"], dq_r, wq), ("dk", res["dk"], dk_r, wk), ("dv", res["dv"], dv_r, wv)):
+        g = got.to(torch.float64).numpy()[w]
+        r = ref[w]
+        assert np.isfinite(g).all(), f"non-finite {name} in a written row"
+        err = float(np.max(np.abs(g - r), initial=0.0)) / max(1.0, float(np.max(np.abs(r), initial=0.0)))
+        errs[name] = err
+        assert err <= tol, f"{name} normalised error {err} > {tol}"
+    # rows outside the sequences and token gaps keep the sentinel
+    for name, back, w, h in (("dq", res["dqb"], wq, batch.h_q), ("dk", res["dkb"], wk, batch.h_kv),
+                             ("dv", res["dvb"], wv, batch.h_kv)):
+        raw = back.view(torch.uint8).numpy().reshape(back.shape[0], -1)
+        assert (raw[~w] == SENTINEL).all(), f"a pad row of {name} was written"
+        assert (raw[w][:, h * batch.d * back.element_size():] == SENTINEL).all(), f"{name} token gap written"
+    return errs
+
+
+SMALL = {
+    "tiny_padded": {},
+    "padded_causal": dict(b=4, h=4, min_len=64, max_len=400),
+    "mixed_gqa": dict(b=6, median=128, max_len=700, total=1900, h_q=8, h_kv=2),
+    "separate_padding": dict(b=6, max_len=500, h=4),
+    "cp_chunks": dict(docs=2, k_len=1024, q_len=384, h=2),
+}
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_bwd_workloads_small(name, kernel):
+    batch = wl.make(name, **SMALL[name])
+    res = run_bwd(batch, kernel=kernel, seed=11)
+    assert res["status"] == 0
+    check_bwd(batch, res)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("seed", range(8))
+def test_bwd_random_packs(seed, kernel):
+    """Ragged packs with mixed masks, causal offsets, windows, GQA, both Stats
+    layouts and per-tensor token gaps on all eight views."""
+    rng = np.random.default_rng(5000 + seed)
+    dtype = ["bf16", "fp16", "fp32"][seed % 3]
+    d = [64, 128, 32, 16][seed % 4]
+    h_kv = int(rng.integers(1, 3))
+    h_q = h_kv * int(rng.integers(1, 4))
+    batch = wl.random_pack(6000 + seed, batch=int(rng.integers(1, 6)), max_len=int(rng.integers(1, 500)),
+                           h_q=h_q, h_kv=h_kv, d=d, dtype=dtype, with_window=bool(seed % 2))
+    gaps = tuple(int(x) for x in rng.integers(0, 3, size=8))
+    res = run_bwd(batch, kernel=kernel, gaps=gaps, seed=seed)
+    assert res["status"] == 0
+    check_bwd(batch, res)
+
+
+def test_bwd_empty_sequences_and_dead_rows():
+    """Sequences with no queries still write dK = dV = 0 for their keys; rows with
+    no visible key write dQ = 0."""
+    # seed chosen so that sequence 4 has 0 queries and 54 keys, and negative causal
+    # offsets leave the first rows of sequences 0, 1 and 3 without a visible key
+    batch = wl.random_pack(7032, batch=5, max_len=90, h_q=2, h_kv=1, d=64, dtype="bf16", masks=(2,),
+                           with_qco=True)
+    assert batch.lens_q()[4] == 0 and batch.lens_k()[4] > 0 and batch.q_causal_offset[0] < 0
+    res = run_bwd(batch, seed=3)
+    assert res["status"] == 0
+    check_bwd(batch, res)
+    k0, n = int(batch.off_k[4]), int(batch.lens_k()[4])
+    assert (res["dk"][k0:k0 + n].float() == 0).all() and (res["dv"][k0:k0 + n].float() == 0).all()
+    q0 = int(batch.off_q[0])
+    dead = -int(batch.q_causal_offset[0])           # rows i < -c see no key
+    assert (res["dq"][q0:q0 + dead].float() == 0).all()
+
+
+def test_bwd_invalid_sequence_flagged_and_untouched():
+    batch = wl.random_pack(7002, batch=4, max_len=100, h_q=2, h_kv=2, d=64, dtype="bf16", allow_empty=False)
+    mask = batch.mask_type.copy()
+    mask[1] = 5
+    res = run_bwd(batch, seed=4, device_mask=mask)
+    assert res["status"] & bd.DEV_BAD_MASK
+    # the bad sequence's gradient rows keep the sentinel
+    for key, off, n in (("dqb", batch.off_q[1], batch.lens_q()[1]), ("dkb", batch.off_k[1], batch.lens_k()[1]),
+                        ("dvb", batch.off_v[1], batch.lens_k()[1])):
+        raw = res[key].view(torch.uint8).numpy().reshape(res[key].shape[0], -1)
+        assert (raw[off:off + n] == SENTINEL).all()
