@@ -30,6 +30,10 @@ int num_sms_of_current_device() {
   return cached[dev];
 }
 
+float scale_of(const thd_attn_desc_t& d) {
+  return std::isnan(d.softmax_scale) ? 1.0f / std::sqrt((float)d.d) : d.softmax_scale;
+}
+
 bool tc_applicable(const thd_attn_desc_t& d, float scale) {
   if (!thd::tc_kernel_available()) return false;
   if (!(scale > 0.f)) return false;  // the softmax takes the row max of unscaled scores
@@ -392,17 +396,30 @@ thd_status_t thd_attn_plan_bwd(thd_attn_plan_t* out, const thd_attn_bwd_desc_t* 
                                                   desc->stride_head[i], eb);
     if (span > desc->bytes[i]) return THD_ERR_CAPACITY;
   }
-  if (d.kernel == THD_KERNEL_TCGEN05) return THD_ERR_UNSUPPORTED;
+  // tensor-core backward: the forward's conditions, plus dO through TMA and 16-byte
+  // gradient rows
+  bool tc_ok = tc_applicable(d, scale_of(d));
+  for (int i = 0; i < 4; ++i) {
+    if (desc->stride_tok[i] <= 0 || desc->stride_head[i] <= 0) tc_ok = false;
+    if ((desc->stride_tok[i] * eb) % 16 != 0 || (desc->stride_head[i] * eb) % 16 != 0) tc_ok = false;
+  }
+  thd_kernel_t kernel;
+  if (d.kernel == THD_KERNEL_SIMT) {
+    kernel = THD_KERNEL_SIMT;
+  } else if (d.kernel == THD_KERNEL_TCGEN05) {
+    if (!tc_ok) return THD_ERR_UNSUPPORTED;
+    kernel = THD_KERNEL_TCGEN05;
+  } else {
+    kernel = tc_ok ? THD_KERNEL_TCGEN05 : THD_KERNEL_SIMT;
+  }
 
   auto* p = new (std::nothrow) thd_attn_plan_s;
   if (!p) return THD_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   p->desc = d;
   p->is_bwd = 1;
-  p->kernel = THD_KERNEL_SIMT;
-  float scale = d.softmax_scale;
-  if (std::isnan(scale)) scale = 1.0f / std::sqrt((float)d.d);
-  p->scale = scale;
+  p->kernel = kernel;
+  p->scale = scale_of(d);
   p->elem_bytes = eb;
   for (int i = 0; i < 4; ++i) {
     p->g_cap_rows[i] = desc->cap_rows[i];
@@ -438,7 +455,7 @@ thd_status_t thd_attn_plan_bwd(thd_attn_plan_t* out, const thd_attn_bwd_desc_t* 
   p->ws_off_b[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
   p->ws_off_b[1] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
   p->ws_off_b[2] = off; off = align_up(off + max_k * (int64_t)sizeof(thd::PairRec), kAlign);
-  p->ws_off_b[3] = off; off = align_up(off + (int64_t)d.h_q * d.cap_rows[0] * 8, kAlign);
+  p->ws_off_b[3] = off; off = align_up(off + max_q * d.h_q * thd::kBwdRowsPerUnit * 8, kAlign);
   p->ws_bytes = (size_t)off;
   *ws_bytes = p->ws_bytes;
   *out = p;
@@ -529,16 +546,35 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   bp.status = const_cast<uint32_t*>(bp.header_q) + thd::kHdrStatus;
   bp.meta = sp.meta;
   bp.ld = reinterpret_cast<float2*>(ws + plan->ws_off_b[3]);
-  bp.ld_rows = d.cap_rows[0];
+  bp.pair_base_q = reinterpret_cast<const int32_t*>(ws + plan->ws_off[2]);
   bp.rows_per_unit = plan->rows_per_unit;
   bp.keys_per_unit = thd::kBwdKeysPerUnit;
   bp.has_window = window_left != nullptr ? 1 : 0;
 
+  // a view with no rows has no TMA descriptor: the SIMT kernels serve that call
+  bool use_tc = plan->kernel == THD_KERNEL_TCGEN05;
+  for (int i = 0; i < 3; ++i)
+    if (d.cap_rows[i] == 0) use_tc = false;
+  if (plan->g_cap_rows[0] == 0) use_tc = false;
+  if (use_tc) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(d_o) |
+                        reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+                        reinterpret_cast<uintptr_t>(dv);
+    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
+  }
   if (thd::launch_bwd_prep(bp, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
   const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
   if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
     return THD_ERR_CUDA;
-  if (thd::launch_bwd_simt(bp, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
+  if (use_tc) {
+    const cudaError_t err = thd::launch_bwd_tc(bp, d, plan->g_cap_rows, plan->g_stride_tok, plan->g_stride_head,
+                                               plan->max_pairs, plan->max_pairs_k, num_sms, stream);
+    if (err == cudaErrorNotSupported) return THD_ERR_UNSUPPORTED;
+    if (err != cudaSuccess) return THD_ERR_CUDA;
+  } else if (thd::launch_bwd_simt(bp, d.dtype, num_sms, stream) != cudaSuccess) {
+    return THD_ERR_CUDA;
+  }
   if (prof) {
     if (cudaEventRecord(plan->prof_events[2 * plan->prof_count + 1], stream) != cudaSuccess)
       return THD_ERR_CUDA;

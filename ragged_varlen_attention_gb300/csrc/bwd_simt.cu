@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(BwdParams p) {
         const float lse = p.stats[(int64_t)(m.off_s + r) * p.stats_tok + (int64_t)h * p.stats_head];
         // a row whose LSE is -inf has no visible key: +inf turns every P of it into 0
         const float l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
-        p.ld[(int64_t)h * p.ld_rows + m.off_q + r] = make_float2(l2, acc);
+        p.ld[ld_index(p.pair_base_q, pr.b, r, h, p.h_q)] = make_float2(l2, acc);
       }
     }
   }
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt_kernel(BwdParams p) {
             q[e] = to_f32(qrow[dbase + e]) * p.scale_log2;
             go[e] = to_f32(grow[dbase + e]);
           }
-        const float2 ld = p.ld[(int64_t)h * p.ld_rows + m.off_q + r];
+        const float2 ld = p.ld[ld_index(p.pair_base_q, pr.b, r, h, p.h_q)];
         l2 = ld.x;
         dsum = ld.y;
       }
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(BwdParams p) {
           }
           if (tid < kRB) {
             const int i = i0 + tid;
-            lds[tid] = i < i_hi ? p.ld[(int64_t)h * p.ld_rows + m.off_q + i] : make_float2(INFINITY, 0.f);
+            lds[tid] = i < i_hi ? p.ld[ld_index(p.pair_base_q, pr.b, i, h, p.h_q)] : make_float2(INFINITY, 0.f);
           }
           __syncthreads();
 #pragma unroll 4

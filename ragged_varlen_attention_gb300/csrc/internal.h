@@ -164,12 +164,19 @@ struct BwdParams {
   const PairRec* pairs_k;
   uint32_t* status;
   const SeqMeta* meta;
-  float2* ld;               // [h_q][ld_rows]: (LSE * log2(e), D = <dO, O>) per query row
-  int64_t ld_rows;          // rows of Q's view: ld index = h * ld_rows + off_q + i
+  const int32_t* pair_base_q;   // [B + 1] first query-axis pair of each sequence (unsorted numbering)
+  // (LSE * log2(e), D = <dO, O>) per query row, in 128-row blocks: row i of sequence b
+  // and head h sits at ld_index(pair_base_q, b, i, h, h_q); each block is 1 KB
+  float2* ld;
   int32_t rows_per_unit;
   int32_t keys_per_unit;
   int32_t has_window;
 };
+
+// index of query row i (of sequence b) and head h in BwdParams::ld
+__device__ __forceinline__ int64_t ld_index(const int32_t* pair_base_q, int b, int i, int h, int h_q) {
+  return ((int64_t)(pair_base_q[b] + i / 128) * h_q + h) * 128 + (i & 127);
+}
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }

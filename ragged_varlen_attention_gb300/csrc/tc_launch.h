@@ -15,4 +15,11 @@ int tc_grid_size(int num_sms, int max_pairs, int h_q);  // persistent CTAs launc
 cudaError_t launch_fwd_tc(const FwdParams& p, const thd_attn_desc_t& desc, int max_pairs, int num_sms,
                           cudaStream_t stream);
 
+// Backward: encodes TMA descriptors for Q, K, V and dO and launches the dQ and
+// dK/dV kernels (after the setup and preprocess kernels). g_* index 0..3 = dO,
+// dQ, dK, dV. Returns cudaErrorNotSupported when a descriptor cannot be encoded.
+cudaError_t launch_bwd_tc(const BwdParams& p, const thd_attn_desc_t& desc, const int64_t g_cap[4],
+                          const int64_t g_stok[4], const int64_t g_shead[4], int max_q, int max_k, int num_sms,
+                          cudaStream_t stream);
+
 }  // namespace thd

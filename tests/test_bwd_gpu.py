@@ -11,6 +11,8 @@ by P_ij * |dO_i| * |O_i| * 2^-9 at most; fp32 1e-4 (fp32 arithmetic throughout).
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -129,6 +131,31 @@ SMALL = {
 def test_bwd_workloads_small(name, kernel):
     batch = wl.make(name, **SMALL[name])
     res = run_bwd(batch, kernel=kernel, seed=11)
+    assert res["status"] == 0
+    if kernel == bd.KERNEL_AUTO and batch.dtype in ("bf16", "fp16") and batch.d in (64, 128):
+        assert res["plan"].kernel == bd.KERNEL_TCGEN05
+    check_bwd(batch, res)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("windows", [None, (300, 0, 1000)])
+def test_bwd_long_sequences(kernel, windows):
+    """Sequences of many 128-row tiles on both axes (causal, so the per-unit tile
+    ranges differ row to row and key to key), with and without windows."""
+    batch = wl.padded_causal(b=3, h=2, min_len=900, max_len=1700)
+    if windows is not None:
+        batch = dataclasses.replace(batch, window_left=np.array(windows, dtype=np.int32))
+    res = run_bwd(batch, kernel=kernel, seed=12)
+    assert res["status"] == 0
+    check_bwd(batch, res)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_gqa_groups_tc(d):
+    """Query-head groups of 4 summed into each kv head's dK/dV by the key-tile kernel."""
+    batch = wl.random_pack(7100 + d, batch=4, max_len=600, h_q=8, h_kv=2, d=d, dtype="bf16",
+                           allow_empty=False)
+    res = run_bwd(batch, kernel=bd.KERNEL_TCGEN05, seed=13)
     assert res["status"] == 0
     check_bwd(batch, res)
 
