@@ -289,6 +289,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kv-split", action="store_true", help="plan with THD_FLAG_NO_KV_SPLIT")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward pass (thd_attn_bwd) instead of the forward")
     ap.add_argument("--window-left", type=int, default=None,
                     help="left window (keys) on every causal sequence, through thd_attn_fwd_window")
     args = ap.parse_args()
@@ -313,6 +315,11 @@ def main():
     if dist is not None:
         dist.barrier()
     kernel = {"auto": bd.KERNEL_AUTO, "simt": bd.KERNEL_SIMT, "tcgen05": bd.KERNEL_TCGEN05}[args.kernel]
+    if args.bwd:
+        bench_backward(args, batch, bd, kernel, device, dist, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     # host (pinned) inputs and device copies
     ints = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt))
@@ -441,6 +448,181 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+BWD_METRIC = "packed-THD attn bwd TFLOP/s (10 * d * unmasked entries: QK^T, dO V^T, P^T dO, dS^T Q, dS K)"
+
+
+def oracle_bwd_sample_time(batch, budget_s: float):
+    """Backward oracle on growing prefixes of sequence 0, head 0 (a crop of the
+    workload: rows [0, R) with the keys they see) until ``budget_s`` elapses.
+    Returns (seconds, algorithmic FLOPs, description)."""
+    from oracle import attention_one_head_bwd, causal_shift, window_lower_shift
+    lq, lk = batch.lens_q(), batch.lens_k()
+    scale = 1.0 / math.sqrt(batch.d) if batch.softmax_scale is None else batch.softmax_scale
+    shift = causal_shift(int(batch.mask_type[0]), int(lq[0]), int(lk[0]),
+                         None if batch.q_causal_offset is None else batch.q_causal_offset[0])
+    lower = window_lower_shift(int(batch.mask_type[0]), shift,
+                               None if batch.window_left is None else batch.window_left[0])
+    rng = np.random.default_rng(0)
+    cap = min(int(lq[0]), 512)            # bounds the [rows, keys] float64 temporaries
+    secs, flops, calls, rows = 0.0, 0, 0, min(64, cap)
+    while secs < budget_s and rows > 0:
+        r = rows
+        kmax = int(lk[0]) if shift is None else max(0, min(int(lk[0]), r - 1 + shift + 1))
+        qb = batch.q[batch.off_q[0]:batch.off_q[0] + r, 0].to(torch.float64).numpy()
+        kb = batch.k[batch.off_k[0]:batch.off_k[0] + kmax, 0].to(torch.float64).numpy()
+        vb = batch.v[batch.off_v[0]:batch.off_v[0] + kmax, 0].to(torch.float64).numpy()
+        gb = rng.standard_normal((r, batch.d))
+        t0 = time.perf_counter()
+        attention_one_head_bwd(qb, kb, vb, gb, scale, shift, lower)
+        secs += time.perf_counter() - t0
+        i = np.arange(r, dtype=np.int64)
+        if shift is None:
+            n = r * kmax
+        else:
+            hi = np.clip(i + shift + 1, 0, kmax)
+            lo = 0 if lower is None else np.clip(i + lower, 0, kmax)
+            n = int(np.maximum(hi - lo, 0).sum())
+        flops += 10 * batch.d * n
+        calls += 1
+        rows = min(2 * rows, cap)
+    desc = (f"{calls} oracle backward calls on the first R rows of sequence 0, head 0 (R doubling from 64 "
+            f"to {cap}, then repeated) with the keys they see, float64 numpy")
+    return secs, flops, desc
+
+
+def bench_backward(args, batch, bd, kernel, device, dist, rank, world):
+    """Backward timing: O and Stats come from this library's forward on the same
+    inputs, dO is seeded N(0, 1); each step is one thd_attn_bwd."""
+    ints = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt))
+    g = torch.Generator().manual_seed(1234)
+    d_o_host = torch.randn((batch.cap_o, batch.h_q, batch.d), generator=g).to(batch.torch_dtype)
+    host = {"q": batch.q.pin_memory(), "k": batch.k.pin_memory(), "v": batch.v.pin_memory(),
+            "d_o": d_o_host.pin_memory(),
+            "cu_q": ints(batch.cu_seqlens_q).pin_memory(), "cu_k": ints(batch.cu_seqlens_kv).pin_memory(),
+            "offs": [ints(x).pin_memory() for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o,
+                                                    batch.off_s)],
+            "mask": ints(batch.mask_type, np.int8).pin_memory(),
+            "qco": None if batch.q_causal_offset is None else ints(batch.q_causal_offset).pin_memory(),
+            "win": None if batch.window_left is None else ints(batch.window_left).pin_memory()}
+    dev = {k: (None if v is None else ([t.to(device) for t in v] if isinstance(v, list) else v.to(device)))
+           for k, v in host.items()}
+    o = torch.zeros((batch.cap_o, batch.h_q, batch.d), dtype=batch.torch_dtype, device=device)
+    stats = torch.zeros((batch.stats_numel,), dtype=torch.float32, device=device)
+    fplan = bd.plan_for_tensors(dev["q"], dev["k"], dev["v"], o, batch.batch, batch.cap_s, batch.stats_layout,
+                                batch.softmax_scale, kernel, 0)
+    fws = bd.alloc_workspace(fplan, device)
+    stream = torch.cuda.current_stream(device)
+    bd.thd_attn_fwd_window(fplan, dev["q"], dev["k"], dev["v"], o, stats, dev["cu_q"], dev["cu_k"], *dev["offs"],
+                           dev["mask"], dev["qco"], dev["win"], fws, stream)
+    if bd.thd_attn_read_status(fplan, fws, stream) != 0:
+        raise SystemExit("device status word set by the forward on the benchmark workload")
+    o_host = o.cpu().pin_memory()
+    stats_host = stats.cpu().pin_memory()
+    dq, dk, dv = (torch.zeros_like(dev[n]) for n in ("q", "k", "v"))
+    dq_host, dk_host, dv_host = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    plan = bd.plan_bwd_for_tensors(dev["q"], dev["k"], dev["v"], o, dev["d_o"], dq, dk, dv, batch.batch,
+                                   batch.cap_s, batch.stats_layout, batch.softmax_scale, kernel, 0)
+    ws = bd.alloc_workspace(plan, device)
+    small_inputs = valid_bytes(batch) * 2 <= 129e6
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device) if small_inputs else None
+
+    def step():
+        bd.thd_attn_bwd(plan, dev["q"], dev["k"], dev["v"], o, dev["d_o"], stats, dq, dk, dv, dev["cu_q"],
+                        dev["cu_k"], *dev["offs"], dev["mask"], dev["qco"], dev["win"], ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    if bd.thd_attn_read_status(plan, ws, stream) != 0:
+        raise SystemExit("device status word set by the backward on the benchmark workload")
+    flop_per_step = 10 * batch.d * unmasked_entries(batch)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else 0
+    sampler = ClockSampler(gpu_index)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bd.profile_enable(plan, args.steps)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(dist, device)
+    total_ms = 0.0
+    if flush is None:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier(dist, device)
+        total_ms = ev0.elapsed_time(ev1)
+    else:
+        for _ in range(args.steps):
+            flush.fill_(1)
+            ev0.record(stream)
+            step()
+            ev1.record(stream)
+            ev1.synchronize()
+            total_ms += ev0.elapsed_time(ev1)
+        barrier(dist, device)
+    clocks = sampler.stop()
+    kernel_ms, kernel_launches = bd.profile_read(plan)
+    bd.profile_enable(plan, 0)
+    ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
+    value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+    h2d_t = [host[n] for n in ("q", "k", "v", "d_o", "cu_q", "cu_k", "mask")] + host["offs"] + [o_host, stats_host]
+    h2d_t += [host[n] for n in ("qco", "win") if host[n] is not None]
+    h2d = sum(t.numel() * t.element_size() for t in h2d_t)
+    d2h = sum(t.numel() * t.element_size() for t in (dq_host, dk_host, dv_host))
+
+    def e2e_step():
+        for name in ("q", "k", "v", "d_o", "cu_q", "cu_k", "mask", "qco", "win"):
+            if host[name] is not None:
+                dev[name].copy_(host[name], non_blocking=True)
+        for dt, ht in zip(dev["offs"], host["offs"]):
+            dt.copy_(ht, non_blocking=True)
+        o.copy_(o_host, non_blocking=True)
+        stats.copy_(stats_host, non_blocking=True)
+        step()
+        for dt, ht in ((dq, dq_host), (dk, dk_host), (dv, dv_host)):
+            ht.copy_(dt, non_blocking=True)
+
+    e2e_step()
+    barrier(dist, device)
+    ev0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    barrier(dist, device)
+    e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / args.e2e_steps, device)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    kernel_tflops = flop_per_step / (kernel_ms * 1e-3) / 1e12 if kernel_ms > 0 else None
+    tc = plan.kernel == bd.KERNEL_TCGEN05
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": batch.dtype, "data": "synthetic",
+        "config": {**config_block(args, batch), "pass": "backward",
+                   "kernel": "tcgen05" if tc else "simt", "flop_per_step": flop_per_step,
+                   "hardware_flop_per_step": (14 if tc else 10) * batch.d * unmasked_entries(batch)},
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": None if kernel_tflops is None else kernel_tflops / peak,
+                     "peak_source": f"bf16_tflops (burst) of {peak_src} MEASURED_PEAKS.json"
+                     if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                     "kernel": "dQ kernel + dK/dV kernel (CUDA events on their stream around both)",
+                     "kernel_ms": kernel_ms, "launches": kernel_launches, "traffic": None},
+        "e2e": {"value": flop_per_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "steps": args.e2e_steps},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, flops, desc = oracle_bwd_sample_time(batch, args.cpu_baseline_seconds)
+        line["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc + f"; {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":
