@@ -306,6 +306,55 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
                           const int32_t* q_causal_offset, const int32_t* window_left,
                           void* workspace, void* stream);
 
+/* ------------------------------------------------------------ indexer top-k
+ *
+ * Sparse-attention indexer over a packed THD batch: per query row, score every
+ * visible key and keep the top-k (Megatron-LM PR #14 "fix(dsa): align packed-CP
+ * indexer causal masks": the indexer masks each THD segment with the same causal
+ * policy as attention, bottom-right with q_causal_offset for context-parallel
+ * chunks, then selects the best keys per row). The pages do not print the score;
+ * this library computes the lightning-indexer score of DeepSeek-V3.2 sparse
+ * attention, with H indexer heads:
+ *
+ *     I_ij = sum_h  w_ih * max(0, <q_ih, k_j>)       (fp32 accumulation)
+ *
+ *   q_i = QI[off_q[b] + i, h, :], k_j = KI[off_k[b] + j, :] (one indexer key per
+ *   token), w_ih = W[off_q[b] + i, h] (float32; any scale folded in). Visible keys
+ *   as in thd_attn_fwd (mask 0 / 1 / 2, q_causal_offset). For each row, idx_out
+ *   row off_out[b] + i receives the sequence-local numbers j of the min(topk,
+ *   visible) visible keys of largest I_ij, ordered by descending score (equal
+ *   scores: ascending j), then -1; score_out (optional) the matching scores, NaN
+ *   in unused slots. Rows outside the sequences are never written.
+ */
+typedef struct {
+  thd_dtype_t dtype;              /* QI and KI storage: THD_BF16 or THD_FP16 */
+  int32_t batch;
+  int32_t heads;                  /* H, 1..128 */
+  int32_t d;                      /* 1..128 */
+  int32_t topk;                   /* 1..2048 */
+  int64_t cap_rows_q, stride_tok_q, stride_head_q;  /* QI view [rows, H, d]; W has the same rows */
+  int64_t cap_rows_k, stride_tok_k;                  /* KI view [rows, d] */
+  int64_t stride_tok_w;           /* float32 W [cap_rows_q, H], head stride 1 */
+  int64_t cap_rows_out;           /* idx_out int32 [rows, topk] and score_out float32 [rows, topk] */
+  int64_t max_seqlen_k;           /* bound on len_k for the score scratch (0 = cap_rows_k); a
+                                     longer sequence sets THD_DEV_BAD_LENGTH and gets no work */
+  thd_kernel_t kernel;
+  uint32_t flags;                 /* none defined; must be 0 */
+} thd_indexer_desc_t;
+
+/* Validate and size (host only). The workspace holds the schedule and a float32
+ * score row of max_seqlen_k entries per output row. */
+thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* desc, size_t* workspace_bytes);
+
+/* Enqueue the indexer top-k (asynchronous, no allocation, no device->host read).
+ * score_out may be NULL. Offsets are row offsets into QI (and W), KI and the
+ * outputs; off_out[b] addresses both idx_out and score_out. */
+thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void* k_i, const float* w,
+                              int32_t* idx_out, float* score_out, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_kv, const int32_t* off_q, const int32_t* off_k,
+                              const int32_t* off_out, const int8_t* mask_type,
+                              const int32_t* q_causal_offset, void* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

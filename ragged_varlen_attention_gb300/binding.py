@@ -62,12 +62,33 @@ class ThdAttnBwdDesc(ctypes.Structure):
     ]
 
 
+class ThdIndexerDesc(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("batch", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("cap_rows_q", ctypes.c_int64),
+        ("stride_tok_q", ctypes.c_int64),
+        ("stride_head_q", ctypes.c_int64),
+        ("cap_rows_k", ctypes.c_int64),
+        ("stride_tok_k", ctypes.c_int64),
+        ("stride_tok_w", ctypes.c_int64),
+        ("cap_rows_out", ctypes.c_int64),
+        ("max_seqlen_k", ctypes.c_int64),
+        ("kernel", ctypes.c_int),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
 _LIB = None
 _EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_plan_kernel",
             "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
             "thd_attn_status_string", "thd_attn_view_span_bytes", "thd_attn_profile_enable",
             "thd_attn_profile_read", "thd_attn_fwd_static_ws", "thd_attn_static_workspace_capacity",
-            "thd_attn_fwd_window", "thd_attn_plan_bwd", "thd_attn_bwd"]
+            "thd_attn_fwd_window", "thd_attn_plan_bwd", "thd_attn_bwd", "thd_indexer_plan",
+            "thd_indexer_topk"]
 
 
 def library_path() -> str:
@@ -96,6 +117,11 @@ def load_library():
     lib.thd_attn_plan_bwd.restype = ctypes.c_int
     lib.thd_attn_bwd.argtypes = [vp] * 22
     lib.thd_attn_bwd.restype = ctypes.c_int
+    lib.thd_indexer_plan.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(ThdIndexerDesc),
+                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.thd_indexer_plan.restype = ctypes.c_int
+    lib.thd_indexer_topk.argtypes = [vp] * 15
+    lib.thd_indexer_topk.restype = ctypes.c_int
     lib.thd_attn_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.thd_attn_read_status.restype = ctypes.c_int
     lib.thd_attn_plan_kernel.argtypes = [vp]
@@ -220,6 +246,44 @@ def plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch: int, cap_rows_stats
     return ThdAttnPlan(handle.value, ws.value, bd.fwd)
 
 
+def indexer_plan_for_tensors(q_i, k_i, w, idx_out, batch: int, topk: int, max_seqlen_k: int = 0,
+                             kernel: int = KERNEL_AUTO) -> ThdAttnPlan:
+    """Indexer plan from QI [rows, H, d], KI [rows, d], W [rows, H] (float32, head
+    stride 1) and the int32 [rows, topk] output (see ``thd_indexer_plan``)."""
+    if q_i.dim() != 3 or q_i.stride(2) != 1 or k_i.dim() != 2 or k_i.stride(1) != 1:
+        raise ValueError("QI must be [rows, H, d] and KI [rows, d] with a contiguous last dim")
+    if w.dtype != torch.float32 or w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("W must be float32 [rows, H] with head stride 1")
+    if idx_out.dtype != torch.int32 or idx_out.dim() != 2 or idx_out.shape[1] != topk or not idx_out.is_contiguous():
+        raise ValueError("idx_out must be a contiguous int32 [rows, topk] tensor")
+    d = ThdIndexerDesc()
+    d.dtype = _DTYPE_CODE[q_i.dtype]
+    d.batch, d.heads, d.d, d.topk = batch, q_i.shape[1], q_i.shape[2], topk
+    d.cap_rows_q, d.stride_tok_q, d.stride_head_q = q_i.shape[0], q_i.stride(0), q_i.stride(1)
+    d.cap_rows_k, d.stride_tok_k = k_i.shape[0], k_i.stride(0)
+    d.stride_tok_w = w.stride(0)
+    d.cap_rows_out = idx_out.shape[0]
+    d.max_seqlen_k = int(max_seqlen_k)
+    d.kernel = int(kernel)
+    d.flags = 0
+    lib = load_library()
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.thd_indexer_plan(ctypes.byref(handle), ctypes.byref(d), ctypes.byref(ws))
+    if st != 0:
+        raise ThdAttnError(st, "thd_indexer_plan")
+    plan = ThdAttnPlan.__new__(ThdAttnPlan)
+    plan.handle, plan.workspace_bytes, plan.desc = handle.value, ws.value, d
+    plan.kernel = lib.thd_attn_plan_kernel(handle.value)
+    a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    lib.thd_attn_plan_geometry(handle.value, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    plan.rows_per_unit, plan.keys_per_tile, plan.max_pairs = a.value, b.value, c.value
+    offs = (ctypes.c_int64 * 4)()
+    lib.thd_attn_plan_workspace_layout(handle.value, offs)
+    plan.workspace_layout = tuple(int(x) for x in offs)
+    return plan
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -270,6 +334,18 @@ def thd_attn_bwd(plan: ThdAttnPlan, q, k, v, o, d_o, stats, dq, dk, dv, cu_seqle
                           _ptr(workspace), _stream_handle(stream))
     if st != 0:
         raise ThdAttnError(st, "thd_attn_bwd")
+
+
+def thd_indexer_topk(plan: ThdAttnPlan, q_i, k_i, w, idx_out, score_out, cu_seqlens_q, cu_seqlens_kv,
+                     off_q, off_k, off_out, mask_type, q_causal_offset, workspace, stream=None) -> None:
+    """Enqueue the indexer top-k (see ``thd_indexer_topk`` in include/thd_attn.h)."""
+    lib = load_library()
+    st = lib.thd_indexer_topk(ctypes.c_void_p(plan.handle), _ptr(q_i), _ptr(k_i), _ptr(w), _ptr(idx_out),
+                              _ptr(score_out), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(off_q),
+                              _ptr(off_k), _ptr(off_out), _ptr(mask_type), _ptr(q_causal_offset),
+                              _ptr(workspace), _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_indexer_topk")
 
 
 def thd_attn_fwd_static_ws(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q,

@@ -252,7 +252,7 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
                                  const int32_t* off_k, const int32_t* off_v, const int32_t* off_o,
                                  const int32_t* off_s, const int8_t* mask, const int32_t* qco,
                                  const int32_t* window_left, void* workspace, void* stream_ptr) {
-  if (!plan || plan->is_bwd) return THD_ERR_INVALID_ARG;
+  if (!plan || plan->is_bwd || plan->is_indexer) return THD_ERR_INVALID_ARG;
   const thd_attn_desc_t& d = plan->desc;
   if (!workspace) return THD_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return THD_ERR_WORKSPACE;
@@ -279,6 +279,7 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
   sp.max_pairs = plan->max_pairs;
   sp.h_q = d.h_q;
   sp.key_axis = 0;
+  sp.max_len_k = 0;
   sp.unit_heads = d.h_q;
   sp.allow_split = plan->allow_split;
   sp.element_offsets = (d.flags & THD_FLAG_ELEMENT_OFFSETS) ? 1 : 0;
@@ -493,6 +494,7 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   sp.cap_s = d.cap_rows_stats;
   sp.batch = d.batch;
   sp.h_q = d.h_q;
+  sp.max_len_k = 0;
   sp.allow_split = 0;
   sp.element_offsets = (d.flags & THD_FLAG_ELEMENT_OFFSETS) ? 1 : 0;
   sp.offset_multiplier = d.offset_multiplier > 0 ? d.offset_multiplier : 1;
@@ -580,6 +582,115 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
       return THD_ERR_CUDA;
     ++plan->prof_count;
   }
+  return THD_OK;
+}
+
+// -------------------------------------------------------------------------- indexer
+
+thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* desc, size_t* ws_bytes) {
+  if (!out || !desc || !ws_bytes) return THD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const thd_indexer_desc_t& d = *desc;
+  if (d.dtype != THD_BF16 && d.dtype != THD_FP16) return THD_ERR_INVALID_ARG;
+  if (d.batch < 0 || d.heads < 1 || d.heads > 128 || d.d < 1 || d.d > 128) return THD_ERR_INVALID_ARG;
+  if (d.topk < 1 || d.topk > thd::kIndexerMaxTopk) return THD_ERR_INVALID_ARG;
+  if (d.flags != 0) return THD_ERR_INVALID_ARG;
+  if (d.kernel != THD_KERNEL_AUTO && d.kernel != THD_KERNEL_SIMT && d.kernel != THD_KERNEL_TCGEN05)
+    return THD_ERR_INVALID_ARG;
+  const int64_t caps[3] = {d.cap_rows_q, d.cap_rows_k, d.cap_rows_out};
+  for (int i = 0; i < 3; ++i)
+    if (caps[i] < 0 || caps[i] >= (int64_t(1) << 31)) return THD_ERR_INVALID_ARG;
+  if (d.stride_tok_q < 0 || d.stride_head_q < 0 || d.stride_tok_k < 0 || d.stride_tok_w < 0 || d.max_seqlen_k < 0)
+    return THD_ERR_INVALID_ARG;
+  if (d.kernel == THD_KERNEL_TCGEN05) return THD_ERR_UNSUPPORTED;
+  auto* p = new (std::nothrow) thd_attn_plan_s;
+  if (!p) return THD_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->is_indexer = 1;
+  p->idesc = d;
+  p->kernel = THD_KERNEL_SIMT;
+  p->elem_bytes = 2;
+  p->rows_per_unit = thd::kIndexerRowsPerUnit;
+  p->keys_per_tile = 128;
+  const int64_t max_k = d.max_seqlen_k > 0 ? d.max_seqlen_k : d.cap_rows_k;
+  p->score_row = align_up(max_k > 0 ? max_k : 1, 128);
+  const int64_t max_pairs = (int64_t)d.batch + (d.cap_rows_out + p->rows_per_unit - 1) / p->rows_per_unit + 1;
+  p->max_pairs = (int32_t)max_pairs;
+  int64_t off = 0;
+  p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
+  p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
+  p->ws_off[2] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
+  p->ws_off[3] = off; off = align_up(off + max_pairs * (int64_t)sizeof(thd::PairRec), kAlign);
+  p->ws_off[4] = p->ws_off[5] = p->ws_off[6] = off;
+  p->ws_off_b[0] = off; off = align_up(off + d.cap_rows_out * p->score_row * 4, kAlign);
+  p->ws_bytes = (size_t)off;
+  *ws_bytes = p->ws_bytes;
+  *out = p;
+  return THD_OK;
+}
+
+thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void* k_i, const float* w,
+                              int32_t* idx_out, float* score_out, const int32_t* cu_q, const int32_t* cu_k,
+                              const int32_t* off_q, const int32_t* off_k, const int32_t* off_out, const int8_t* mask,
+                              const int32_t* qco, void* workspace, void* stream_ptr) {
+  if (!plan || !plan->is_indexer) return THD_ERR_INVALID_ARG;
+  const thd_indexer_desc_t& d = plan->idesc;
+  if (!workspace) return THD_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return THD_ERR_WORKSPACE;
+  if (d.batch > 0 && (!cu_q || !cu_k || !off_q || !off_k || !off_out || !mask)) return THD_ERR_INVALID_ARG;
+  if ((!q_i || !w) && d.cap_rows_q > 0) return THD_ERR_INVALID_ARG;
+  if (!k_i && d.cap_rows_k > 0) return THD_ERR_INVALID_ARG;
+  if (!idx_out && d.cap_rows_out > 0) return THD_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  const int num_sms = num_sms_of_current_device();
+  if (num_sms <= 0) return THD_ERR_CUDA;
+  thd::SetupParams sp;
+  sp.cu_q = cu_q; sp.cu_k = cu_k;
+  sp.off_q = off_q; sp.off_k = off_k; sp.off_v = off_k; sp.off_o = off_out; sp.off_s = off_out;
+  sp.mask = mask; sp.qco = qco; sp.window = nullptr;
+  sp.cap_q = d.cap_rows_q; sp.cap_k = d.cap_rows_k; sp.cap_v = d.cap_rows_k; sp.cap_o = d.cap_rows_out;
+  sp.cap_s = d.cap_rows_out;
+  sp.batch = d.batch;
+  sp.rows_per_unit = plan->rows_per_unit;
+  sp.keys_per_tile = plan->keys_per_tile;
+  sp.max_pairs = plan->max_pairs;
+  sp.h_q = 1;
+  sp.key_axis = 0;
+  sp.max_len_k = d.max_seqlen_k;   // 0: len_k <= cap_rows_k <= the score row already
+  sp.unit_heads = 1;
+  sp.allow_split = 0;
+  sp.element_offsets = 0;
+  sp.offset_multiplier = 1;
+  for (int i = 0; i < 5; ++i) sp.tok_stride[i] = 1;
+  sp.num_ctas = num_sms;
+  sp.max_split = 0;
+  sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
+  sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
+  sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
+  sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
+  sp.splits = nullptr;
+  if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
+  thd::IndexerParams ip;
+  ip.q = q_i; ip.k = k_i; ip.w = w; ip.idx = idx_out; ip.score_out = score_out;
+  ip.scores = reinterpret_cast<float*>(ws + plan->ws_off_b[0]);
+  ip.q_tok = d.stride_tok_q; ip.q_head = d.stride_head_q; ip.k_tok = d.stride_tok_k; ip.w_tok = d.stride_tok_w;
+  ip.score_row = plan->score_row;
+  ip.heads = d.heads; ip.d = d.d; ip.topk = d.topk;
+  ip.header = sp.header;
+  ip.counter = sp.header + thd::kHdrCounter;
+  ip.pairs = sp.pairs;
+  ip.meta = sp.meta;
+  ip.status = sp.header + thd::kHdrStatus;
+  const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
+  if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
+    return THD_ERR_CUDA;
+  if (thd::launch_indexer_scores_simt(ip, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
+  if (prof) {
+    if (cudaEventRecord(plan->prof_events[2 * plan->prof_count + 1], stream) != cudaSuccess) return THD_ERR_CUDA;
+    ++plan->prof_count;
+  }
+  if (thd::launch_indexer_topk(ip, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
   return THD_OK;
 }
 

@@ -78,6 +78,7 @@ struct SetupParams {
   int32_t max_pairs;        // pairs before splitting
   int32_t h_q;
   int32_t key_axis;         // 0: units over query rows (cost = KV tiles); 1: over keys (cost = query tiles)
+  int64_t max_len_k;        // > 0: a longer key sequence is a BAD_LENGTH data error
   int32_t unit_heads;       // heads each pair is scheduled for (h_q, or h_kv on the key axis)
   int32_t allow_split;      // KV split permitted (workspace holds the partial buffers)
   int32_t element_offsets;  // offsets are elements (x multiplier): divide by the token strides
@@ -173,6 +174,28 @@ struct BwdParams {
   int32_t has_window;
 };
 
+// Arguments of the indexer kernels (scores, then per-row top-k).
+struct IndexerParams {
+  const void* q;            // QI [rows, H, d]
+  const void* k;            // KI [rows, d]
+  const float* w;           // W [rows of QI, H]
+  int32_t* idx;             // [rows, topk]
+  float* score_out;         // [rows, topk] or null
+  float* scores;            // workspace: score_row floats per output row
+  int64_t q_tok, q_head, k_tok, w_tok;
+  int64_t score_row;
+  int32_t heads, d, topk;
+  const uint32_t* header;
+  uint32_t* counter;
+  const PairRec* pairs;
+  const SeqMeta* meta;
+  uint32_t* status;
+};
+cudaError_t launch_indexer_scores_simt(const IndexerParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
+cudaError_t launch_indexer_topk(const IndexerParams& p, int num_sms, cudaStream_t stream);
+constexpr int kIndexerRowsPerUnit = 128;
+constexpr int kIndexerMaxTopk = 2048;
+
 // index of query row i (of sequence b) and head h in BwdParams::ld
 __device__ __forceinline__ int64_t ld_index(const int32_t* pair_base_q, int b, int i, int h, int h_q) {
   return ((int64_t)(pair_base_q[b] + i / 128) * h_q + h) * 128 + (i & 127);
@@ -216,6 +239,10 @@ struct thd_attn_plan_s {
   int64_t g_stride_head[4];
   int32_t max_pairs_k;      // key-axis pair capacity
   int64_t ws_off_b[4];      // key-axis header, pair_base, pairs; (LSE, D) rows
+  // indexer plans (thd_indexer_plan): ws_off[0..3] as above, ws_off_b[0] the score rows
+  int32_t is_indexer;
+  thd_indexer_desc_t idesc;
+  int64_t score_row;        // floats per output row in the score scratch
   // optional attention-kernel timing (thd_attn_profile_enable)
   int32_t prof_slots;
   int32_t prof_count;

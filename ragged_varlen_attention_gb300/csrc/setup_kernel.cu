@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
       }
       m.off_q = rows[0]; m.off_k = rows[1]; m.off_v = rows[2]; m.off_o = rows[3]; m.off_s = rows[4];
       const int mt = (int)p.mask[b];
-      if (lq < 0 || lk < 0) bad |= THD_DEV_BAD_LENGTH;
+      if (lq < 0 || lk < 0 || (p.max_len_k > 0 && lk > p.max_len_k)) bad |= THD_DEV_BAD_LENGTH;
       if (mt < 0 || mt > 2) bad |= THD_DEV_BAD_MASK;
       if (!bad) {
         auto in_cap = [](int32_t off, int32_t len, int64_t cap) {

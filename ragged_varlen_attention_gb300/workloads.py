@@ -275,3 +275,86 @@ def random_pack(seed: int, *, batch: int = 4, max_len: int = 200, h_q: int = 4, 
     return ThdBatch(f"random_pack_{seed}", dtype, h_q, h_kv, d, _cumsum0(lq), _cumsum0(lk),
                     off_q, off_k, off_k.copy(), off_q.copy(), off_q.copy(), mask, qco,
                     stats_layout, q, k, v, cap_q, cap_q, window_left=window)
+
+
+# ------------------------------------------------------------------- indexer inputs
+@dataclass
+class IndexerBatch:
+    """Packed inputs of the sparse-attention indexer top-k: QI [cap_q, H, d],
+    KI [cap_k, d], W [cap_q, H] float32 (rows addressed like QI's), and the
+    output rows ``off_out`` of an int32 [cap_out, topk] index tensor."""
+    name: str
+    dtype: str
+    heads: int
+    d: int
+    topk: int
+    cu_seqlens_q: np.ndarray
+    cu_seqlens_kv: np.ndarray
+    off_q: np.ndarray
+    off_k: np.ndarray
+    off_out: np.ndarray
+    mask_type: np.ndarray
+    q_causal_offset: np.ndarray | None
+    q: torch.Tensor
+    k: torch.Tensor
+    w: torch.Tensor
+    cap_out: int
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_seqlens_q) - 1
+
+    def lens_q(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_q)
+
+    def lens_k(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_kv)
+
+
+def indexer_cp(seed: int = 106, docs: int = 2, k_len: int = 65536, q_len: int = 4096, heads: int = 64,
+               d: int = 128, topk: int = 2048, dtype: str = "bf16") -> IndexerBatch:
+    """Context-parallel indexer chunks (the Megatron-LM PR #14 multi-document case):
+    per document a packed key prefix of ``k_len`` tokens and a ``q_len``-row query
+    chunk at causal offset k_len - q_len (bottom-right), N(0,1) indexer vectors,
+    weights N(0,1)/sqrt(H)."""
+    rng = np.random.default_rng(seed)
+    lq = np.full(docs, q_len, dtype=np.int64)
+    lk = np.full(docs, k_len, dtype=np.int64)
+    off_q = _cumsum0(lq)[:-1].astype(np.int32)
+    off_k = _cumsum0(lk)[:-1].astype(np.int32)
+    q = _normal(rng, (int(lq.sum()), heads, d), dtype)
+    k = _normal(rng, (int(lk.sum()), d), dtype)
+    w = torch.from_numpy((rng.standard_normal((int(lq.sum()), heads)) / np.sqrt(heads)).astype(np.float32))
+    return IndexerBatch("indexer_cp", dtype, heads, d, topk, _cumsum0(lq), _cumsum0(lk), off_q, off_k,
+                        off_q.copy(), np.full(docs, MASK_BOTTOM_RIGHT, dtype=np.int8),
+                        (lk - lq).astype(np.int32), q, k, w, int(lq.sum()))
+
+
+def indexer_random_pack(seed: int, *, batch: int = 4, max_len: int = 300, heads: int = 4, d: int = 64,
+                        topk: int = 16, dtype: str = "bf16", masks=(0, 1, 2), max_gap: int = 5,
+                        zero_q_rows: int = 0) -> IndexerBatch:
+    """Small random indexer pack: ragged lengths, gaps in QI, KI and the output,
+    mixed masks and causal offsets; ``zero_q_rows`` rows get q = 0 (every score 0:
+    the selection is decided by the tie order alone)."""
+    rng = np.random.default_rng(seed)
+    lq = rng.integers(0, max_len, size=batch, endpoint=True)
+    lk = rng.integers(0, max_len, size=batch, endpoint=True)
+    gq = rng.integers(0, max_gap, size=batch, endpoint=True)
+    gk = rng.integers(0, max_gap, size=batch, endpoint=True)
+    go = rng.integers(0, max_gap, size=batch, endpoint=True)
+    off_q = (_cumsum0(lq + gq) + 1).astype(np.int32)[:-1]
+    off_k = (_cumsum0(lk + gk) + 2).astype(np.int32)[:-1]
+    off_o = (_cumsum0(lq + go) + 3).astype(np.int32)[:-1]
+    cap_q = int(off_q[-1] + lq[-1] + 2) if batch else 1
+    cap_k = int(off_k[-1] + lk[-1] + 2) if batch else 1
+    cap_o = int(off_o[-1] + lq[-1] + 2) if batch else 1
+    q = _normal(rng, (cap_q, heads, d), dtype)
+    k = _normal(rng, (cap_k, d), dtype)
+    w = torch.from_numpy(rng.standard_normal((cap_q, heads)).astype(np.float32))
+    if zero_q_rows:
+        rows = rng.choice(cap_q, size=min(zero_q_rows, cap_q), replace=False)
+        q[torch.from_numpy(rows)] = 0
+    mask = rng.choice(np.array(masks, dtype=np.int8), size=batch)
+    qco = np.array([int(rng.integers(-2, int(b_) + 3)) for b_ in lk], dtype=np.int32)
+    return IndexerBatch(f"indexer_random_{seed}", dtype, heads, d, topk, _cumsum0(lq), _cumsum0(lk),
+                        off_q, off_k, off_o, mask, qco, q, k, w, cap_o)

@@ -1,0 +1,134 @@
+"""GPU parity of the indexer top-k against the CPU indexer oracle.
+
+The kernel accumulates scores in fp32 (bf16/fp16 products are exact in fp32), the
+oracle in fp64: near-equal scores may order differently. So the comparison is by
+score, per row, with tau = 1e-3 * (1 + max |I_ij|) (fp32 accumulation over H*d
+terms stays orders of magnitude below): the count is min(k, visible keys), every
+index is a distinct visible key, every selected key scores >= the oracle's k-th
+score - tau, every visible key scoring > k-th + tau is selected, the returned
+scores match the oracle's within tau and are non-increasing, and rows outside
+the sequences keep their sentinel. Where every score of a row is exactly 0 (q = 0)
+the tie order decides alone and the indices must equal the oracle's exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.indexer as ix
+from oracle.thd_attention import causal_shift
+from ragged_varlen_attention_gb300 import binding as bd
+from ragged_varlen_attention_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SENT = -7
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from ragged_varlen_attention_gb300 import build
+    build.build()
+    bd.load_library()
+
+
+def run_indexer(batch: wl.IndexerBatch, kernel=bd.KERNEL_AUTO, max_seqlen_k=0, device="cuda"):
+    q, k, w = batch.q.to(device), batch.k.to(device), batch.w.to(device)
+    idx = torch.full((batch.cap_out, batch.topk), SENT, dtype=torch.int32, device=device)
+    sc = torch.full((batch.cap_out, batch.topk), -123.0, dtype=torch.float32, device=device)
+    ints = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    mask = torch.from_numpy(np.ascontiguousarray(batch.mask_type, dtype=np.int8)).to(device)
+    qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
+    plan = bd.indexer_plan_for_tensors(q, k, w, idx, batch.batch, batch.topk, max_seqlen_k, kernel)
+    ws = bd.alloc_workspace(plan, device)
+    bd.thd_indexer_topk(plan, q, k, w, idx, sc, ints(batch.cu_seqlens_q), ints(batch.cu_seqlens_kv),
+                        ints(batch.off_q), ints(batch.off_k), ints(batch.off_out), mask, qco, ws)
+    status = bd.thd_attn_read_status(plan, ws)
+    torch.cuda.synchronize()
+    return dict(idx=idx.cpu().numpy(), scores=sc.cpu().numpy(), status=status, plan=plan)
+
+
+def check_indexer(batch: wl.IndexerBatch, res, exact_rows=False):
+    init = np.full((batch.cap_out, batch.topk), SENT, dtype=np.int64)
+    ref_idx, ref_sel, written = ix.indexer_topk(
+        batch.q.to(torch.float64).numpy(), batch.k.to(torch.float64).numpy(), batch.w.to(torch.float64).numpy(),
+        batch.cu_seqlens_q, batch.cu_seqlens_kv, batch.off_q, batch.off_k, batch.off_out, batch.mask_type,
+        batch.q_causal_offset, batch.topk, init)
+    got, got_s = res["idx"], res["scores"]
+    assert (got[~written] == SENT).all(), "an output row outside the sequences was written"
+    assert (got_s[~written] == -123.0).all()
+    lq, lk = batch.lens_q(), batch.lens_k()
+    q64, k64, w64 = (t.to(torch.float64).numpy() for t in (batch.q, batch.k, batch.w))
+    for b in range(batch.batch):
+        if lq[b] == 0:
+            continue
+        qs, ks, os_ = int(batch.off_q[b]), int(batch.off_k[b]), int(batch.off_out[b])
+        S = ix.indexer_scores_one(q64[qs:qs + lq[b]], k64[ks:ks + lk[b]], w64[qs:qs + lq[b]])
+        shift = causal_shift(int(batch.mask_type[b]), int(lq[b]), int(lk[b]),
+                             None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+        for i in range(int(lq[b])):
+            n_vis = int(lk[b]) if shift is None else max(0, min(int(lk[b]), i + shift + 1))
+            row, srow = got[os_ + i], got_s[os_ + i]
+            n_out = min(batch.topk, n_vis)
+            assert (row[:n_out] >= 0).all() and (row[n_out:] == -1).all(), f"seq {b} row {i}: count"
+            sel = row[:n_out]
+            assert len(set(sel.tolist())) == n_out and (sel < n_vis).all(), f"seq {b} row {i}: bad index"
+            assert np.isnan(srow[n_out:]).all()
+            if n_out == 0:
+                continue
+            vis_scores = S[i, :n_vis]
+            tau = 1e-3 * (1.0 + float(np.abs(vis_scores).max()))
+            kth = float(ref_sel[os_ + i, n_out - 1])
+            assert (S[i, sel] >= kth - tau).all(), f"seq {b} row {i}: a selected key scores below the k-th"
+            must = np.nonzero(vis_scores > kth + tau)[0]
+            assert set(must.tolist()) <= set(sel.tolist()), f"seq {b} row {i}: a clearly better key is missing"
+            assert np.abs(srow[:n_out] - S[i, sel]).max() <= tau
+            assert (np.diff(srow[:n_out]) <= 0).all(), f"seq {b} row {i}: not in descending order"
+            if exact_rows and not np.any(q64[qs + i]):
+                assert list(sel) == list(ref_idx[os_ + i, :n_out]), f"seq {b} row {i}: tie order"
+
+
+@pytest.mark.parametrize("topk", [1, 16, 200])
+def test_indexer_cp_chunks_small(topk):
+    """Two documents, bottom-right causal query chunks at q_causal_offset = k_len - q_len."""
+    batch = wl.indexer_cp(docs=2, k_len=1100, q_len=300, heads=8, d=64, topk=topk)
+    res = run_indexer(batch)
+    assert res["status"] == 0
+    check_indexer(batch, res)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_indexer_random_packs(seed):
+    rng = np.random.default_rng(8000 + seed)
+    heads = [1, 4, 16, 64][seed % 4]
+    d = [64, 128, 32, 16][(seed // 2) % 4]
+    topk = [1, 7, 128, 300, 2048][seed % 5]
+    batch = wl.indexer_random_pack(8100 + seed, batch=int(rng.integers(1, 6)), max_len=int(rng.integers(1, 700)),
+                                   heads=heads, d=d, topk=topk, dtype=["bf16", "fp16"][seed % 2],
+                                   zero_q_rows=5)
+    res = run_indexer(batch)
+    assert res["status"] == 0
+    check_indexer(batch, res, exact_rows=True)
+
+
+def test_indexer_long_rows_full_topk():
+    """Rows of up to 3000 visible keys with k = 2048 (the radix-select path with a
+    large k), plus rows with fewer visible keys than k."""
+    batch = wl.indexer_random_pack(8200, batch=2, max_len=3000, heads=4, d=64, topk=2048, masks=(0, 2))
+    res = run_indexer(batch)
+    assert res["status"] == 0
+    check_indexer(batch, res)
+
+
+def test_indexer_key_length_over_bound_is_flagged():
+    batch = wl.indexer_random_pack(8300, batch=3, max_len=200, heads=2, d=32, topk=8)
+    lk = batch.lens_k()
+    res = run_indexer(batch, max_seqlen_k=int(lk.max()) - 1)
+    assert res["status"] & bd.DEV_BAD_LENGTH
+    # the long sequence's rows are untouched
+    b = int(np.argmax(lk))
+    o, n = int(batch.off_out[b]), int(batch.lens_q()[b])
+    assert (res["idx"][o:o + n] == SENT).all()
