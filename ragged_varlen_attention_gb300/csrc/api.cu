@@ -602,20 +602,24 @@ thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* de
     if (caps[i] < 0 || caps[i] >= (int64_t(1) << 31)) return THD_ERR_INVALID_ARG;
   if (d.stride_tok_q < 0 || d.stride_head_q < 0 || d.stride_tok_k < 0 || d.stride_tok_w < 0 || d.max_seqlen_k < 0)
     return THD_ERR_INVALID_ARG;
-  if (d.kernel == THD_KERNEL_TCGEN05) return THD_ERR_UNSUPPORTED;
+  const bool tc_ok = thd::indexer_tc_applicable(d);
+  if (d.kernel == THD_KERNEL_TCGEN05 && !tc_ok) return THD_ERR_UNSUPPORTED;
   auto* p = new (std::nothrow) thd_attn_plan_s;
   if (!p) return THD_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   p->is_indexer = 1;
   p->idesc = d;
-  p->kernel = THD_KERNEL_SIMT;
+  p->kernel = (d.kernel != THD_KERNEL_SIMT && tc_ok) ? THD_KERNEL_TCGEN05 : THD_KERNEL_SIMT;
   p->elem_bytes = 2;
   p->rows_per_unit = thd::kIndexerRowsPerUnit;
   p->keys_per_tile = 128;
-  const int64_t max_k = d.max_seqlen_k > 0 ? d.max_seqlen_k : d.cap_rows_k;
-  p->score_row = align_up(max_k > 0 ? max_k : 1, 128);
+  const int64_t max_len = d.max_seqlen_k > 0 ? d.max_seqlen_k : d.cap_rows_k;
+  p->score_row = align_up(max_len > 0 ? max_len : 1, 128);
   const int64_t max_pairs = (int64_t)d.batch + (d.cap_rows_out + p->rows_per_unit - 1) / p->rows_per_unit + 1;
   p->max_pairs = (int32_t)max_pairs;
+  // key-axis units (tensor-core scores): non-overlapping key rows bound them
+  const int64_t max_k = (int64_t)d.batch + (d.cap_rows_k + 127) / 128 + 1;
+  p->max_pairs_k = (int32_t)max_k;
   int64_t off = 0;
   p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
   p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
@@ -623,6 +627,9 @@ thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* de
   p->ws_off[3] = off; off = align_up(off + max_pairs * (int64_t)sizeof(thd::PairRec), kAlign);
   p->ws_off[4] = p->ws_off[5] = p->ws_off[6] = off;
   p->ws_off_b[0] = off; off = align_up(off + d.cap_rows_out * p->score_row * 4, kAlign);
+  p->ws_off_b[1] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
+  p->ws_off_b[2] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
+  p->ws_off_b[3] = off; off = align_up(off + max_k * (int64_t)sizeof(thd::PairRec), kAlign);
   p->ws_bytes = (size_t)off;
   *ws_bytes = p->ws_bytes;
   *out = p;
@@ -671,21 +678,50 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
   sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
   sp.splits = nullptr;
   if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
+  bool use_tc = plan->kernel == THD_KERNEL_TCGEN05 && d.cap_rows_q > 0 && d.cap_rows_k > 0;
+  if (use_tc) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q_i) | reinterpret_cast<uintptr_t>(k_i) |
+                        reinterpret_cast<uintptr_t>(w);
+    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
+  }
   thd::IndexerParams ip;
+  ip.header_k = nullptr;
+  ip.counter_k = nullptr;
+  ip.pairs_k = nullptr;
+  if (use_tc) {
+    // key-axis schedule for the tensor-core scores (units of 128 keys)
+    sp.key_axis = 1;
+    sp.rows_per_unit = 128;
+    sp.keys_per_tile = 128;
+    sp.max_pairs = plan->max_pairs_k;
+    sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off_b[1]);
+    sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off_b[2]);
+    sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off_b[3]);
+    if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
+    ip.header_k = sp.header;
+    ip.counter_k = sp.header + thd::kHdrCounter;
+    ip.pairs_k = sp.pairs;
+  }
   ip.q = q_i; ip.k = k_i; ip.w = w; ip.idx = idx_out; ip.score_out = score_out;
   ip.scores = reinterpret_cast<float*>(ws + plan->ws_off_b[0]);
   ip.q_tok = d.stride_tok_q; ip.q_head = d.stride_head_q; ip.k_tok = d.stride_tok_k; ip.w_tok = d.stride_tok_w;
   ip.score_row = plan->score_row;
   ip.heads = d.heads; ip.d = d.d; ip.topk = d.topk;
-  ip.header = sp.header;
-  ip.counter = sp.header + thd::kHdrCounter;
-  ip.pairs = sp.pairs;
+  ip.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
+  ip.counter = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]) + thd::kHdrCounter;
+  ip.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
   ip.meta = sp.meta;
-  ip.status = sp.header + thd::kHdrStatus;
+  ip.status = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]) + thd::kHdrStatus;
   const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
   if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
     return THD_ERR_CUDA;
-  if (thd::launch_indexer_scores_simt(ip, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
+  if (use_tc) {
+    const cudaError_t err = thd::launch_indexer_scores_tc(ip, d, plan->max_pairs_k, num_sms, stream);
+    if (err == cudaErrorNotSupported) return THD_ERR_UNSUPPORTED;
+    if (err != cudaSuccess) return THD_ERR_CUDA;
+  } else if (thd::launch_indexer_scores_simt(ip, d.dtype, num_sms, stream) != cudaSuccess) {
+    return THD_ERR_CUDA;
+  }
   if (prof) {
     if (cudaEventRecord(plan->prof_events[2 * plan->prof_count + 1], stream) != cudaSuccess) return THD_ERR_CUDA;
     ++plan->prof_count;

@@ -190,6 +190,10 @@ struct IndexerParams {
   const PairRec* pairs;
   const SeqMeta* meta;
   uint32_t* status;
+  // key-axis schedule (tensor-core scores: units of 128 keys)
+  const uint32_t* header_k;
+  uint32_t* counter_k;
+  const PairRec* pairs_k;
 };
 cudaError_t launch_indexer_scores_simt(const IndexerParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
 cudaError_t launch_indexer_topk(const IndexerParams& p, int num_sms, cudaStream_t stream);

@@ -92,5 +92,19 @@ inline bool encode_view(CUtensorMap* map, const void* base, bool bf16, int d, in
   return r == CUDA_SUCCESS;
 }
 
+// general tiled map: `rank` dims (innermost first) with byte strides of the outer
+// dims, a box, and a swizzle mode; rows past a dim read as zeros
+inline bool encode_tiled(CUtensorMap* map, const void* base, CUtensorMapDataType type, int rank,
+                         const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                         CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, type, (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace tc_host
 }  // namespace thd

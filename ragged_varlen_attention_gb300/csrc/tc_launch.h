@@ -22,4 +22,11 @@ cudaError_t launch_bwd_tc(const BwdParams& p, const thd_attn_desc_t& desc, const
                           const int64_t g_stok[4], const int64_t g_shead[4], int max_q, int max_k, int num_sms,
                           cudaStream_t stream);
 
+// Indexer scores on the tensor cores: units of 128 keys (key-axis schedule in
+// p.header_k), H in {4, 8, 16, 32, 64}, d in {64, 128}. cudaErrorNotSupported when
+// the shape or a descriptor is not served.
+bool indexer_tc_applicable(const thd_indexer_desc_t& d);
+cudaError_t launch_indexer_scores_tc(const IndexerParams& p, const thd_indexer_desc_t& desc, int max_pairs_k,
+                                     int num_sms, cudaStream_t stream);
+
 }  // namespace thd

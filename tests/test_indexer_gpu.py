@@ -91,13 +91,27 @@ def check_indexer(batch: wl.IndexerBatch, res, exact_rows=False):
                 assert list(sel) == list(ref_idx[os_ + i, :n_out]), f"seq {b} row {i}: tie order"
 
 
+@pytest.mark.parametrize("kernel", [bd.KERNEL_AUTO, bd.KERNEL_SIMT])
 @pytest.mark.parametrize("topk", [1, 16, 200])
-def test_indexer_cp_chunks_small(topk):
+def test_indexer_cp_chunks_small(topk, kernel):
     """Two documents, bottom-right causal query chunks at q_causal_offset = k_len - q_len."""
     batch = wl.indexer_cp(docs=2, k_len=1100, q_len=300, heads=8, d=64, topk=topk)
-    res = run_indexer(batch)
+    res = run_indexer(batch, kernel=kernel)
     assert res["status"] == 0
+    if kernel == bd.KERNEL_AUTO:
+        assert res["plan"].kernel == bd.KERNEL_TCGEN05
     check_indexer(batch, res)
+
+
+@pytest.mark.parametrize("heads,d", [(4, 64), (8, 128), (16, 64), (32, 128), (64, 128), (64, 64)])
+def test_indexer_tc_shapes(heads, d):
+    """Tensor-core scores for every supported head count (R = 128 / H query rows per
+    MMA), ragged packs with gaps, mixed masks and ties."""
+    batch = wl.indexer_random_pack(8400 + heads + d, batch=4, max_len=700, heads=heads, d=d, topk=64,
+                                   dtype="bf16" if heads % 16 else "fp16", zero_q_rows=4)
+    res = run_indexer(batch, kernel=bd.KERNEL_TCGEN05)
+    assert res["status"] == 0
+    check_indexer(batch, res, exact_rows=True)
 
 
 @pytest.mark.parametrize("seed", range(8))
