@@ -289,6 +289,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kv-split", action="store_true", help="plan with THD_FLAG_NO_KV_SPLIT")
+    ap.add_argument("--indexer", action="store_true",
+                    help="time the indexer top-k (thd_indexer_topk) on the context-parallel indexer workload")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass (thd_attn_bwd) instead of the forward")
     ap.add_argument("--window-left", type=int, default=None,
@@ -297,6 +299,9 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     from ragged_varlen_attention_gb300 import workloads as wl
+    if args.indexer:
+        bench_indexer(args)
+        return
     batch = wl.make(args.workload)
     if args.window_left is not None:
         import dataclasses
@@ -623,6 +628,159 @@ def bench_backward(args, batch, bd, kernel, device, dist, rank, world):
                                 "kind": "oracle", "sample": desc + f"; {secs:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+IDX_METRIC = "packed-THD indexer top-k TFLOP/s (2 * H * d per visible (row, key) pair)"
+IDX_DESC = ("context-parallel indexer chunks: 2 docs x 65536 keys, a 4096-row query chunk per doc at "
+            "q_causal_offset = k_len - q_len (bottom-right causal), H=64 indexer heads, d=128, bf16, "
+            "W ~ N(0,1)/sqrt(H) float32, top-2048 per row")
+
+
+def indexer_visible_pairs(b) -> int:
+    lq, lk = b.lens_q(), b.lens_k()
+    total = 0
+    for s_ in range(b.batch):
+        mt = int(b.mask_type[s_])
+        if mt == 0:
+            total += int(lq[s_]) * int(lk[s_])
+            continue
+        c = 0 if mt == 1 else (int(lk[s_] - lq[s_]) if b.q_causal_offset is None else int(b.q_causal_offset[s_]))
+        i = np.arange(int(lq[s_]), dtype=np.int64)
+        total += int(np.clip(i + c + 1, 0, int(lk[s_])).sum())
+    return total
+
+
+def oracle_indexer_sample_time(b, budget_s: float):
+    """Indexer oracle on rows of document 0 (growing prefixes of the chunk, each row
+    against its visible keys) until ``budget_s`` elapses."""
+    from oracle import indexer_scores_one, select_topk
+    q64 = b.q[:int(b.lens_q()[0])].to(torch.float64).numpy()
+    k64 = b.k[:int(b.lens_k()[0])].to(torch.float64).numpy()
+    w64 = b.w[:int(b.lens_q()[0])].to(torch.float64).numpy()
+    c = int(b.q_causal_offset[0])
+    secs, flops, rows_done, r0 = 0.0, 0, 0, 0
+    while secs < budget_s and r0 < q64.shape[0]:
+        r1 = min(q64.shape[0], r0 + 8)
+        kmax = min(k64.shape[0], r1 - 1 + c + 1)
+        t0 = time.perf_counter()
+        sc = indexer_scores_one(q64[r0:r1], k64[:kmax], w64[r0:r1])
+        vis = np.arange(kmax)[None, :] <= (np.arange(r0, r1)[:, None] + c)
+        select_topk(sc, vis, b.topk)
+        secs += time.perf_counter() - t0
+        flops += 2 * b.heads * b.d * int(vis.sum())
+        rows_done += r1 - r0
+        r0 = r1
+    return secs, flops, f"{rows_done} query rows of document 0 (8 rows per oracle call, each against its visible keys), float64 numpy"
+
+
+def bench_indexer(args):
+    from ragged_varlen_attention_gb300 import binding as bd
+    from ragged_varlen_attention_gb300 import build
+    from ragged_varlen_attention_gb300 import workloads as wl
+    dist, rank, world, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0 or not os.path.exists(bd.library_path()):
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    kernel = {"auto": bd.KERNEL_AUTO, "simt": bd.KERNEL_SIMT, "tcgen05": bd.KERNEL_TCGEN05}[args.kernel]
+    b = wl.indexer_cp()
+    ints = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt))
+    host = {"q": b.q.pin_memory(), "k": b.k.pin_memory(), "w": b.w.pin_memory(),
+            "cu_q": ints(b.cu_seqlens_q).pin_memory(), "cu_k": ints(b.cu_seqlens_kv).pin_memory(),
+            "off_q": ints(b.off_q).pin_memory(), "off_k": ints(b.off_k).pin_memory(),
+            "off_o": ints(b.off_out).pin_memory(), "mask": ints(b.mask_type, np.int8).pin_memory(),
+            "qco": ints(b.q_causal_offset).pin_memory()}
+    dev = {n: t.to(device) for n, t in host.items()}
+    idx = torch.empty((b.cap_out, b.topk), dtype=torch.int32, device=device)
+    sc = torch.empty((b.cap_out, b.topk), dtype=torch.float32, device=device)
+    idx_host = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    sc_host = torch.empty(sc.shape, dtype=sc.dtype).pin_memory()
+    plan = bd.indexer_plan_for_tensors(dev["q"], dev["k"], dev["w"], idx, b.batch, b.topk,
+                                       int(b.lens_k().max()), kernel)
+    ws = bd.alloc_workspace(plan, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        bd.thd_indexer_topk(plan, dev["q"], dev["k"], dev["w"], idx, sc, dev["cu_q"], dev["cu_k"], dev["off_q"],
+                            dev["off_k"], dev["off_o"], dev["mask"], dev["qco"], ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    if bd.thd_attn_read_status(plan, ws, stream) != 0:
+        raise SystemExit("device status word set on the indexer workload")
+    pairs = indexer_visible_pairs(b)
+    flop_per_step = 2 * b.heads * b.d * pairs
+    sampler = ClockSampler(0)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bd.profile_enable(plan, args.steps)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(dist, device)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier(dist, device)
+    total_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop()
+    kernel_ms, launches = bd.profile_read(plan)
+    bd.profile_enable(plan, 0)
+    ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
+    value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = idx_host.numel() * 4 + sc_host.numel() * 4
+
+    def e2e_step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        step()
+        idx_host.copy_(idx, non_blocking=True)
+        sc_host.copy_(sc, non_blocking=True)
+
+    e2e_step()
+    barrier(dist, device)
+    ev0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    barrier(dist, device)
+    e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / args.e2e_steps, device)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    kt = flop_per_step / (kernel_ms * 1e-3) / 1e12 if kernel_ms > 0 else None
+    tc = plan.kernel == bd.KERNEL_TCGEN05
+    line = {
+        "metric": IDX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": b.dtype, "data": "synthetic",
+        "config": {"workload": IDX_DESC, "name": "indexer_cp", "heads": b.heads, "d": b.d, "topk": b.topk,
+                   "visible_pairs": pairs, "flop_per_step": flop_per_step, "pass": "indexer",
+                   "kernel": "tcgen05" if tc else "simt",
+                   "l2": "inputs smaller than L2 but the float32 score scratch (2 GB) is not; no flush",
+                   "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"},
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": kt, "peak": peak, "unit": "TFLOP/s",
+                     "frac": None if kt is None else kt / peak,
+                     "peak_source": f"bf16_tflops (burst) of {peak_src} MEASURED_PEAKS.json"
+                     if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                     "kernel": "indexer score kernel (CUDA events on its stream)",
+                     "kernel_ms": kernel_ms, "launches": launches, "traffic": None},
+        "e2e": {"value": flop_per_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "steps": args.e2e_steps},
+        "gpu_launches": (4 if tc else 3) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, flops, desc = oracle_indexer_sample_time(b, args.cpu_baseline_seconds)
+        line["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc + f"; {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
