@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
   BwUnit* info = reinterpret_cast<BwUnit*>(smem + C::kOffInfo);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 4);
-  const Sync sy{sbase + (uint32_t)C::kOffBar, abort_flag, p.status};
+  // short spins before the sleep-hinted waits: a softmax warp that polls long
+  // takes issue slots from the warps (and the issuing thread) on its sub-partition
+  const Sync sy{sbase + (uint32_t)C::kOffBar, abort_flag, p.status, 4};
   const Ring ring{C::kStages};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -563,7 +565,9 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
   BwUnit* info = reinterpret_cast<BwUnit*>(smem + C::kOffInfo);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 4);
-  const Sync sy{sbase + (uint32_t)C::kOffBar, abort_flag, p.status};
+  // short spins before the sleep-hinted waits: a softmax warp that polls long
+  // takes issue slots from the warps (and the issuing thread) on its sub-partition
+  const Sync sy{sbase + (uint32_t)C::kOffBar, abort_flag, p.status, 4};
   const Ring ring{C::kStages};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

@@ -19,6 +19,7 @@ struct Sync {
   uint32_t bar0;               // shared address of barrier 0
   volatile int* abort_flag;
   uint32_t* status;
+  int spins = 96;              // non-blocking probes before the sleep-hinted waits
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
   // bounded wait for the phase of `parity` on barrier i; false on abort/timeout
   __device__ __forceinline__ bool wait(int i, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) const {
@@ -26,7 +27,7 @@ struct Sync {
     // short spin of non-blocking probes (wake-up latency matters on the critical
     // path), then sleep-hinted blocking tries so long waits leave the issue slots
     // to other warps
-    for (int k = 0; k < 96; ++k)
+    for (int k = 0; k < spins; ++k)
       if (ptx::mbar_test_wait(b, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {
@@ -75,15 +76,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows, heads, d] view, box = 64 d-elements x 1 head x 128 rows, 128-byte swizzle;
-// rows past `rows` read as zeros
+// [rows, heads, d] view, box = 64 d-elements x 1 head x box_rows rows, 128-byte
+// swizzle; rows past `rows` read as zeros
 inline bool encode_view(CUtensorMap* map, const void* base, bool bf16, int d, int64_t heads, int64_t rows,
-                 int64_t stride_head, int64_t stride_tok) {
+                 int64_t stride_head, int64_t stride_tok, int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)(stride_head * 2), (cuuint64_t)(stride_tok * 2)};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
