@@ -443,6 +443,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     __syncwarp();
   } else {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
+    // softmax warps poll briefly before the sleep-hinted waits: long polling takes
+    // issue slots from the MMA-issuing and TMA threads on the same sub-partitions
+    const Sync sw{sy.bar0, sy.abort_flag, sy.status, 4};
     // ---------------------------------------------------------- softmax, per sub-tile
     // Warpgroup t owns query rows [row0 + 128 t, row0 + 128 t + 128) of the unit:
     // its threads turn S_t into P_t in TMEM, rescale O_t when the running max
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = (int)(it & 1u);
-      if (!sy.wait_warp(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
+      if (!sw.wait_warp(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
       const UnitInfo u = info[slot];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        if (!(ok = sy.wait_warp(B_S_FULL + t, (s_cnt++) & 1u))) break;
+        if (!(ok = sw.wait_warp(B_S_FULL + t, (s_cnt++) & 1u))) break;
         ptx::tc_fence_after();
         uint32_t s[4][32];
 #pragma unroll
@@ -592,7 +595,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       float* prow = p.part_o + (((int64_t)u.part_slot * p.h_q + u.h) * p.rows_per_unit + urow) * D;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (n > 0) {
-        if (!sy.wait_warp(B_O_FULL + t, (o_cnt++) & 1u)) break;
+        if (!sw.wait_warp(B_O_FULL + t, (o_cnt++) & 1u)) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
