@@ -29,7 +29,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(thd_attn_[a-z_0-9]+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(thd_(?:attn|indexer)_[a-z_0-9]+)\s*\(",
                                  text, flags=re.M)))
 
 
@@ -162,3 +162,89 @@ def test_unit_order_covers_every_pair_and_head_once():
     # units (query heads 0-3) for pairs 1 and 2 before kv head 1's
     assert order[:8] == [(0, h) for h in range(4)] + [(0, h) for h in range(4, 8)]
     assert order[8:16] == [(1, 0), (1, 1), (1, 2), (1, 3), (2, 0), (2, 1), (2, 2), (2, 3)]
+
+
+# ------------------------------------------------------------------ backward plans
+def _bwd_desc(grad_caps=(100, 100, 80, 80), grad_tok=(512, 512, 256, 256), nbytes=(0, 0, 0, 0), **kw):
+    bdesc = bd.ThdAttnBwdDesc()
+    bdesc.fwd = _desc(**kw)
+    for i in range(4):
+        bdesc.cap_rows[i] = grad_caps[i]
+        bdesc.stride_tok[i] = grad_tok[i]
+        bdesc.stride_head[i] = 128
+        bdesc.bytes[i] = nbytes[i]
+    return bdesc
+
+
+def _plan_bwd(bdesc):
+    lib = bd.load_library()
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.thd_attn_plan_bwd(ctypes.byref(h), ctypes.byref(bdesc), ctypes.byref(ws))
+    kernel = lib.thd_attn_plan_kernel(h) if st == 0 else None
+    if st == 0:
+        lib.thd_attn_plan_destroy(h)
+    return st, ws.value, kernel
+
+
+def test_plan_bwd_validation_and_kernel_choice(lib):
+    st, ws, kernel = _plan_bwd(_bwd_desc())
+    assert st == 0 and ws % 256 == 0 and kernel == bd.KERNEL_TCGEN05
+    # a gradient view with fewer rows than its primal view
+    assert _plan_bwd(_bwd_desc(grad_caps=(100, 99, 80, 80)))[0] == 1
+    # dQ allocation one element short of its all-axes span
+    assert _plan_bwd(_bwd_desc(nbytes=(0, 100 * 512 * 2 - 2, 0, 0)))[0] == 4
+    # forward checks still apply
+    assert _plan_bwd(_bwd_desc(h_q=3, h_kv=2))[0] == 1
+    assert _plan_bwd(_bwd_desc(dtype=torch.float32))[2] == bd.KERNEL_SIMT
+    assert _plan_bwd(_bwd_desc(d=96, kernel=bd.KERNEL_TCGEN05))[0] == 2
+    # a gradient token stride that is not a multiple of 16 bytes keeps the SIMT path
+    assert _plan_bwd(_bwd_desc(grad_tok=(512, 516, 256, 256)))[2] == bd.KERNEL_SIMT
+
+
+def test_fwd_rejects_backward_and_indexer_plans(lib):
+    st, _, _ = _plan_bwd(_bwd_desc())
+    assert st == 0
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    assert lib.thd_attn_plan_bwd(ctypes.byref(h), ctypes.byref(_bwd_desc()), ctypes.byref(ws)) == 0
+    args = [h] + [ctypes.c_void_p(256)] * 15 + [ctypes.c_void_p(0)]
+    assert lib.thd_attn_fwd(*args) == 1
+    lib.thd_attn_plan_destroy(h)
+
+
+# ------------------------------------------------------------------- indexer plans
+def _ix_desc(**kw):
+    d = bd.ThdIndexerDesc()
+    base = dict(dtype=0, batch=2, heads=64, d=128, topk=2048, cap_rows_q=8192, stride_tok_q=64 * 128,
+                stride_head_q=128, cap_rows_k=131072, stride_tok_k=128, stride_tok_w=64, cap_rows_out=8192,
+                max_seqlen_k=65536, kernel=bd.KERNEL_AUTO, flags=0)
+    base.update(kw)
+    for k_, v_ in base.items():
+        setattr(d, k_, v_)
+    return d
+
+
+def _plan_ix(desc):
+    lib = bd.load_library()
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib.thd_indexer_plan(ctypes.byref(h), ctypes.byref(desc), ctypes.byref(ws))
+    kernel = lib.thd_attn_plan_kernel(h) if st == 0 else None
+    if st == 0:
+        lib.thd_attn_plan_destroy(h)
+    return st, ws.value, kernel
+
+
+def test_indexer_plan_validation_and_sizing(lib):
+    st, ws, kernel = _plan_ix(_ix_desc())
+    assert st == 0 and kernel == bd.KERNEL_TCGEN05
+    # one float32 score row of max_seqlen_k (rounded to 128) per output row
+    assert ws >= 8192 * 65536 * 4
+    assert _plan_ix(_ix_desc(max_seqlen_k=1000))[1] < ws
+    for kw in (dict(heads=0), dict(heads=129), dict(topk=0), dict(topk=4096), dict(d=0), dict(flags=1),
+               dict(batch=-1), dict(dtype=2)):
+        assert _plan_ix(_ix_desc(**kw))[0] == 1, kw
+    assert _plan_ix(_ix_desc(heads=2))[2] == bd.KERNEL_SIMT          # H must be 4..64 for tensor cores
+    assert _plan_ix(_ix_desc(heads=2, kernel=bd.KERNEL_TCGEN05))[0] == 2
+    assert _plan_ix(_ix_desc(d=96))[2] == bd.KERNEL_SIMT
