@@ -468,13 +468,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     for (uint32_t it = 0;; ++it) {
       const int slot = (int)(it & 1u);
       if (!sw.wait_warp(B_SCHED_FULL + slot, (it >> 1) & 1u)) break;
+      // the slot stays claimed until the epilogue, which reads its fields again
+      // instead of keeping them in registers through the tile loop
       const UnitInfo u = info[slot];
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
       if (u.w >= num_tiles) break;
       const int n = t ? u.n_kv[1] : u.n_kv[0];
       const int nrows = t ? u.n_rows[1] : u.n_rows[0];
-      if (nrows == 0) continue;
+      if (nrows == 0) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
+        continue;
+      }
       const int r = u.row0 + t * BM + row;      // row inside the sequence
       const bool live = row < nrows;
       const int kmax_row = (int)max64(0, min64((int64_t)u.len_k, (int64_t)r + u.shift + 1));
@@ -589,10 +593,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // epilogue: O = O_acc / l on live rows, LSE = (m + log2 l) * ln 2; dead rows 0 / -inf.
       // For half of a split pair the normalised partial O (fp32) and its base-2 LSE
       // go to the partial buffers instead; the combine kernel merges the halves.
-      const bool partial = u.part_slot >= 0;
+      const volatile UnitInfo* ui = info + slot;
+      const int e_part = ui->part_slot, e_off_o = ui->off_o, e_h = ui->h, e_off_s = ui->off_s;
+      const int er = ui->row0 + t * BM + row;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
+      const bool partial = e_part >= 0;
       const int urow = t * BM + row;            // row within the unit
-      T* orow = O + (int64_t)(u.off_o + r) * p.stride_tok[3] + (int64_t)u.h * p.stride_head[3];
-      float* prow = p.part_o + (((int64_t)u.part_slot * p.h_q + u.h) * p.rows_per_unit + urow) * D;
+      T* orow = O + (int64_t)(e_off_o + er) * p.stride_tok[3] + (int64_t)e_h * p.stride_head[3];
+      float* prow = p.part_o + (((int64_t)e_part * p.h_q + e_h) * p.rows_per_unit + urow) * D;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (n > 0) {
         if (!sw.wait_warp(B_O_FULL + t, (o_cnt++) & 1u)) break;
@@ -631,11 +640,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
       }
       if (live && partial) {
-        p.part_lse[((int64_t)u.part_slot * p.h_q + u.h) * p.rows_per_unit + urow] =
+        p.part_lse[((int64_t)e_part * p.h_q + e_h) * p.rows_per_unit + urow] =
             l > 0.f ? m + ptx::lg2(l) : -INFINITY;
       } else if (live) {
         const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994530942f : -INFINITY;
-        p.stats[(int64_t)(u.off_s + r) * p.stats_tok + (int64_t)u.h * p.stats_head] = lse;
+        p.stats[(int64_t)(e_off_s + er) * p.stats_tok + (int64_t)e_h * p.stats_head] = lse;
       }
     }
   }
