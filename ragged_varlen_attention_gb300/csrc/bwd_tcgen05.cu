@@ -694,8 +694,10 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
           const int zr = nk * 16 - valid;
           if (!(ok = sy.wait(B_P_DONE, (p_waits++) & 1u))) break;
           while (ok && i == 0 && acc_read_waits < acc_reads_seen) ok = sy.wait(B_ACC_READ, (acc_read_waits++) & 1u);
-          // dP(i) has read dO_i before its tail rows are cleared
-          ok = ok && sy.wait(B_DP_FULL, (dp_waits++) & 1u);
+          // dP(i) has read dO_i before its tail rows are cleared (only the last query
+          // tile of a sequence has a tail; the phase count advances every step)
+          const uint32_t dp_phase = dp_waits++;
+          if (zr > 0) ok = ok && sy.wait(B_DP_FULL, dp_phase & 1u);
           if (!ok) break;
           if (zr > 0) {
             zero_rows<C::kHalves>(smem + C::kOffRing + ring.stage(of) * C::kTileBytes, valid, zr);
