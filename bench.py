@@ -368,13 +368,17 @@ def main():
     sampler.start()
     time.sleep(0.3)
     barrier(dist, device)
+    step_ms = []
     if flush is None:
-        ev0.record(stream)
-        for _ in range(args.steps):
+        # one event between consecutive steps: the total and each step's duration
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evs[0].record(stream)
+        for i in range(args.steps):
             step()
-        ev1.record(stream)
+            evs[i + 1].record(stream)
         barrier(dist, device)
-        total_ms = ev0.elapsed_time(ev1)
+        total_ms = evs[0].elapsed_time(evs[-1])
+        step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     else:
         # L2 flushed between steps; only the fwd calls are inside the timed events
         total_ms = 0.0
@@ -384,13 +388,53 @@ def main():
             step()
             ev1.record(stream)
             ev1.synchronize()
-            total_ms += ev0.elapsed_time(ev1)
+            step_ms.append(ev0.elapsed_time(ev1))
+            total_ms += step_ms[-1]
         barrier(dist, device)
     clocks = sampler.stop()
     kernel_ms, kernel_launches = bd.profile_read(plan)
     bd.profile_enable(plan, 0)
     ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
     value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+    # the same step replayed from a CUDA graph (the call is capturable: no host
+    # synchronisation, no allocation)
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            bd.thd_attn_fwd_window(plan, dev["q"], dev["k"], dev["v"], o, stats, dev["cu_q"], dev["cu_k"],
+                                   *dev["offs"], dev["mask"], dev["qco"], dev["win"], ws, cap)
+        cap.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            bd.thd_attn_fwd_window(plan, dev["q"], dev["k"], dev["v"], o, stats, dev["cu_q"], dev["cu_k"],
+                                   *dev["offs"], dev["mask"], dev["qco"], dev["win"], ws, cap)
+        torch.cuda.synchronize(device)
+        g.replay()
+        torch.cuda.synchronize(device)
+        gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if flush is None:
+            gs.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            ge.record(stream)
+            ge.synchronize()
+            graph_ms = gs.elapsed_time(ge) / args.steps
+        else:
+            # as in the timed loop: L2 flushed before each replay, outside the events
+            acc = 0.0
+            for _ in range(args.steps):
+                flush.fill_(1)
+                gs.record(stream)
+                g.replay()
+                ge.record(stream)
+                ge.synchronize()
+                acc += gs.elapsed_time(ge)
+            graph_ms = acc / args.steps
+    except RuntimeError as exc:          # capture unsupported here: report why, keep the line
+        graph_ms = f"unavailable: {exc}".splitlines()[0][:200]
 
     # end-to-end through the public API: pinned host inputs -> device -> fwd -> host outputs
     h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"], host["cu_q"],
@@ -423,6 +467,22 @@ def main():
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     kernel_tflops = flop_per_step / (kernel_ms * 1e-3) / 1e12 if kernel_ms > 0 else None
+    # below the ridge (peak FLOP/s over HBM bytes/s) a launch is bound by HBM: report GB/s
+    bytes_per_step = valid_bytes(batch)
+    ridge = peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    hbm_bound = flop_per_step / max(bytes_per_step, 1) < ridge
+    src = (f"of {peak_src} MEASURED_PEAKS.json" if peak_src == "measured" else "fallback")
+    if hbm_bound:
+        achieved = bytes_per_step / (kernel_ms * 1e-3) / 1e9 if kernel_ms > 0 else None
+        roof = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": None if achieved is None else achieved / float(peaks["hbm_gbs"]),
+                "peak_source": f"hbm_gbs {src}", "bytes_per_launch": bytes_per_step,
+                "arithmetic_intensity": flop_per_step / max(bytes_per_step, 1), "ridge": ridge}
+    else:
+        roof = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": None if kernel_tflops is None else kernel_tflops / peak,
+                "peak_source": f"bf16_tflops (burst) {src}" if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                "arithmetic_intensity": flop_per_step / max(bytes_per_step, 1), "ridge": ridge}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -432,14 +492,14 @@ def main():
                    "kv_split_allowed": plan.kernel == bd.KERNEL_TCGEN05 and not args.no_kv_split,
                    "flop_per_step": flop_per_step},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
-        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": None if kernel_tflops is None else kernel_tflops / peak,
-                     "peak_source": f"bf16_tflops (burst) of {peak_src} MEASURED_PEAKS.json"
-                     if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+        "roofline": {**roof,
                      "kernel": "attention kernel alone (CUDA events on its stream)",
                      "kernel_ms": kernel_ms, "launches": kernel_launches,
-                     "traffic": recorded_traffic(args.workload) if plan.kernel == bd.KERNEL_TCGEN05 else None,
+                     "traffic": recorded_traffic(args.workload) if plan.kernel == bd.KERNEL_TCGEN05
+                     and args.window_left is None else None,
                      "traffic_unit": "bytes per launch (ncu dram read+write)"},
+        "step_ms_median": statistics.median(step_ms) if step_ms else None,
+        "graph_replay_ms_per_step": graph_ms,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": args.e2e_steps},
         "gpu_launches": (3 if plan.kernel == bd.KERNEL_TCGEN05 and not args.no_kv_split else 2) * args.steps,
