@@ -438,3 +438,99 @@ def thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=
     thd_attn_fwd_window(plan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
                         off_o, off_s, mask_type, q_causal_offset, window_left, workspace, stream)
     return o, stats
+
+
+def thd_attn_backward(q, k, v, o, d_o, stats, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=None,
+                      off_v=None, off_o=None, off_s=None, mask_type=None, q_causal_offset=None,
+                      window_left=None, dq=None, dk=None, dv=None, stats_layout: int = STATS_TOKEN_MAJOR,
+                      softmax_scale=None, kernel: int = KERNEL_AUTO, workspace=None, stream=None):
+    """One-call backward over device tensors (``thd_attn_bwd``): the gradients of
+    the forward whose O and Stats are given, for the upstream gradient ``d_o``.
+    Offsets and masks default as in :func:`thd_attn_forward`; gradients are
+    allocated zero-filled when not given. Returns ``(dq, dk, dv)``."""
+    batch = cu_seqlens_q.numel() - 1
+    dev = q.device
+    off_q = cu_seqlens_q if off_q is None else off_q
+    off_k = cu_seqlens_kv if off_k is None else off_k
+    off_v = off_k if off_v is None else off_v
+    off_o = off_q if off_o is None else off_o
+    off_s = off_o if off_s is None else off_s
+    if mask_type is None:
+        mask_type = torch.zeros(max(batch, 1), dtype=torch.int8, device=dev)
+    dq = torch.zeros_like(q) if dq is None else dq
+    dk = torch.zeros_like(k) if dk is None else dk
+    dv = torch.zeros_like(v) if dv is None else dv
+    cap_s = stats.numel() // q.shape[1]
+    key = ("bwd", q.dtype, batch, tuple(q.shape), tuple(k.shape), tuple(v.shape), tuple(o.shape),
+           q.stride(), k.stride(), v.stride(), o.stride(), d_o.stride(), dq.stride(), dk.stride(), dv.stride(),
+           tuple(d_o.shape), tuple(dq.shape), tuple(dk.shape), tuple(dv.shape), cap_s, stats_layout,
+           softmax_scale, kernel)
+    plan = _PLAN_CACHE.get(key)
+    if plan is None:
+        plan = plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch, cap_s, stats_layout, softmax_scale, kernel)
+        _PLAN_CACHE[key] = plan
+    if workspace is None:
+        workspace = alloc_workspace(plan, dev)
+    thd_attn_bwd(plan, q, k, v, o, d_o, stats, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
+                 off_o, off_s, mask_type, q_causal_offset, window_left, workspace, stream)
+    return dq, dk, dv
+
+
+def thd_indexer(q_i, k_i, w, cu_seqlens_q, cu_seqlens_kv, topk: int, *, off_q=None, off_k=None,
+                off_out=None, mask_type=None, q_causal_offset=None, max_seqlen_k: int = 0,
+                idx_out=None, score_out=None, with_scores: bool = True, kernel: int = KERNEL_AUTO,
+                workspace=None, stream=None):
+    """One-call indexer top-k (``thd_indexer_topk``) over device tensors: QI
+    [rows, H, d], KI [rows, d], W float32 [rows, H]. Outputs have QI's rows unless
+    given. Returns ``(idx int32 [rows, topk], scores float32 [rows, topk] or None)``."""
+    batch = cu_seqlens_q.numel() - 1
+    dev = q_i.device
+    off_q = cu_seqlens_q if off_q is None else off_q
+    off_k = cu_seqlens_kv if off_k is None else off_k
+    off_out = off_q if off_out is None else off_out
+    if mask_type is None:
+        mask_type = torch.zeros(max(batch, 1), dtype=torch.int8, device=dev)
+    if idx_out is None:
+        idx_out = torch.full((q_i.shape[0], topk), -1, dtype=torch.int32, device=dev)
+    if score_out is None and with_scores:
+        score_out = torch.full((idx_out.shape[0], topk), float("nan"), dtype=torch.float32, device=dev)
+    key = ("indexer", q_i.dtype, batch, tuple(q_i.shape), q_i.stride(), tuple(k_i.shape), k_i.stride(),
+           w.stride(), tuple(idx_out.shape), topk, max_seqlen_k, kernel)
+    plan = _PLAN_CACHE.get(key)
+    if plan is None:
+        plan = indexer_plan_for_tensors(q_i, k_i, w, idx_out, batch, topk, max_seqlen_k, kernel)
+        _PLAN_CACHE[key] = plan
+    if workspace is None:
+        workspace = alloc_workspace(plan, dev)
+    thd_indexer_topk(plan, q_i, k_i, w, idx_out, score_out, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_out,
+                     mask_type, q_causal_offset, workspace, stream)
+    return idx_out, score_out
+
+
+class ThdAttention(torch.autograd.Function):
+    """Packed-THD attention as an autograd function: forward through
+    ``thd_attn_fwd_window``, backward through ``thd_attn_bwd`` (the caller's
+    metadata tensors are saved, not copied). Use :func:`thd_attention`."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens_q, cu_seqlens_kv, meta: dict):
+        o, stats = thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, **meta)
+        ctx.save_for_backward(q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv)
+        ctx.meta = meta
+        return o
+
+    @staticmethod
+    def backward(ctx, d_o):
+        q, k, v, o, stats, cu_q, cu_k = ctx.saved_tensors
+        m = dict(ctx.meta)
+        for name in ("o", "stats", "workspace"):   # the forward's buffers; the backward sizes its own
+            m.pop(name, None)
+        dq, dk, dv = thd_attn_backward(q, k, v, o, d_o.contiguous(), stats, cu_q, cu_k, **m)
+        return dq, dk, dv, None, None, None
+
+
+def thd_attention(q, k, v, cu_seqlens_q, cu_seqlens_kv, **meta):
+    """Differentiable packed-THD attention: ``meta`` takes the keyword arguments of
+    :func:`thd_attn_forward` (offsets, mask_type, q_causal_offset, window_left,
+    stats_layout, softmax_scale, kernel). Returns O; gradients flow to q, k, v."""
+    return ThdAttention.apply(q, k, v, cu_seqlens_q, cu_seqlens_kv, meta)
