@@ -618,7 +618,7 @@ thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* de
   const int64_t max_pairs = (int64_t)d.batch + (d.cap_rows_out + p->rows_per_unit - 1) / p->rows_per_unit + 1;
   p->max_pairs = (int32_t)max_pairs;
   // key-axis units (tensor-core scores): non-overlapping key rows bound them
-  const int64_t max_k = (int64_t)d.batch + (d.cap_rows_k + 127) / 128 + 1;
+  const int64_t max_k = (int64_t)d.batch + (d.cap_rows_k + thd::kIndexerKeysPerUnit - 1) / thd::kIndexerKeysPerUnit + 1;
   p->max_pairs_k = (int32_t)max_k;
   int64_t off = 0;
   p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
@@ -689,9 +689,9 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
   ip.counter_k = nullptr;
   ip.pairs_k = nullptr;
   if (use_tc) {
-    // key-axis schedule for the tensor-core scores (units of 128 keys)
+    // key-axis schedule for the tensor-core scores (units of 256 keys)
     sp.key_axis = 1;
-    sp.rows_per_unit = 128;
+    sp.rows_per_unit = thd::kIndexerKeysPerUnit;
     sp.keys_per_tile = 128;
     sp.max_pairs = plan->max_pairs_k;
     sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off_b[1]);

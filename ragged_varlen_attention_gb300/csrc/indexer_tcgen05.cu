@@ -3,15 +3,17 @@
 // pair (Megatron-LM PR #14 "fix(dsa): align packed-CP indexer causal masks": the
 // causal policy and q_causal_offset of the packed context-parallel chunks).
 //
-// Unit = 128 keys of one sequence (key-axis schedule, longest first). The key tile
-// K [128 keys x d] stays in shared memory; the query rows that see any of its
-// keys stream through a ring in groups of R = 128 / H rows with all H heads, so
-// one tcgen05.mma chain S^T = K Q'^T (M = 128 keys, N = 128 (row, head) pairs,
-// K = d) fills 128 TMEM columns per group. The score warps own one key each
-// (TMEM lane) and 64 (row, head) columns, so the reduction over heads,
-// sum_h w_ih max(0, s), stays inside the thread; a warp stores 32 consecutive
-// keys of a row (128 bytes). Two TMEM buffers let the MMA of group s + 1 run
-// while group s is reduced.
+// Unit = 256 keys of one sequence (key-axis schedule, longest first), two 128-key
+// sub-tiles K_0, K_1 [128 keys x d] resident in shared memory; the query rows that
+// see any of its keys stream through a ring in groups of R = 128 / H rows with all
+// H heads, and each streamed group feeds two tcgen05.mma chains S^T_t = K_t Q'^T
+// (M = 128 keys, N = 128 (row, head) pairs, K = d): the group tile (32 KB at
+// d = 128) is the large operand, so serving 256 keys per load halves the L2 traffic
+// per FLOP. The score warps own one key of each sub-tile (TMEM lane) and 64
+// (row, head) columns, so the reduction over heads, sum_h w_ih max(0, s), stays
+// inside the thread; a warp stores 32 consecutive keys of a row (128 bytes). Two
+// TMEM buffers (256 columns each) let the MMAs of group s + 1 run while group s is
+// reduced.
 //
 // TMA: Q' as a {64 d, H heads, R rows} box of the [rows, H, d] view (128-byte
 // swizzle: the box lands as 128 rows of 128 bytes, row = r * H + h, the same
@@ -51,9 +53,9 @@ struct IxCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;    // K tile, Q' tile
   static constexpr int kWBytes = R * H * 4;         // 512
-  static constexpr int kStages = D == 128 ? 5 : 10;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffRing = kTileBytes;
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kOffK = 0;                   // K_0, K_1
+  static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffW = kOffRing + kStages * kTileBytes;
   static constexpr int kOffBar = kOffW + kStages * kWBytes;
   static constexpr int kNumBars = B_RING + 2 * kStages;
@@ -81,7 +83,7 @@ __device__ __forceinline__ IxUnit make_unit_ix(const IndexerParams& p, uint32_t 
   const PairRec pr = p.pairs_k[pair];
   const SeqMeta m = p.meta[pr.b];
   u.b = pr.b; u.k0 = pr.row0;
-  u.n_keys = max(0, min(128, m.len_k - pr.row0));
+  u.n_keys = max(0, min(kIndexerKeysPerUnit, m.len_k - pr.row0));
   u.len_q = m.len_q; u.len_k = m.len_k; u.shift = m.shift;
   u.off_q = m.off_q; u.off_k = m.off_k; u.off_o = m.off_o;
   // rows that see a key of the tile: i >= k0 - shift
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(kThreadsIx, 1)
     ptx::prefetch_tmap(&tm_w);
   }
   if (warp == kAllocWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 256);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -157,10 +159,13 @@ __global__ void __launch_bounds__(kThreadsIx, 1)
         if (u.n_steps == 0) continue;
         if (!sy.wait(B_IN_EMPTY, (in_uses & 1u) ^ 1u)) break;
         ++in_uses;
-        ptx::mbar_arrive_expect_tx(sy.bar(B_IN_FULL), C::kTileBytes);
+        ptx::mbar_arrive_expect_tx(sy.bar(B_IN_FULL), 2 * C::kTileBytes);
 #pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          ptx::tma_load_2d(sbase + C::kOffK + hf * 128 * 128, &tm_k, sy.bar(B_IN_FULL), hf * 64, u.off_k + u.k0);
+        for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            ptx::tma_load_2d(sbase + C::kOffK + kt * C::kTileBytes + hf * 128 * 128, &tm_k, sy.bar(B_IN_FULL),
+                             hf * 64, u.off_k + u.k0 + kt * 128);
         bool ok = true;
         for (int s = 0; s < u.n_steps; ++s) {
           const int st = (int)(fill % S);
@@ -216,9 +221,13 @@ __global__ void __launch_bounds__(kThreadsIx, 1)
           ptx::tc_fence_after();
           const uint64_t qa = dq + (uint64_t)((st * C::kTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
-            ptx::mma_ss(tmem + (uint32_t)(b * 128), dk + off, qa + off, idesc, kk > 0 ? 1u : 0u);
+          for (int kt = 0; kt < 2; ++kt) {
+            const uint64_t ka = dk + (uint64_t)((kt * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
+              ptx::mma_ss(tmem + (uint32_t)(b * 256 + kt * 128), ka + off, qa + off, idesc, kk > 0 ? 1u : 0u);
+            }
           }
           ptx::tc_commit(sy.bar(B_S_FULL + b));
           ++uses[b];
@@ -247,8 +256,6 @@ __global__ void __launch_bounds__(kThreadsIx, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
       if (u.w >= num_tiles) break;
-      const int j = u.k0 + row;
-      const bool live = row < u.n_keys;
       bool ok = true;
       for (int s = 0; s < u.n_steps; ++s, ++fill, ++gstep) {
         const int st = (int)(fill % S);
@@ -256,35 +263,49 @@ __global__ void __launch_bounds__(kThreadsIx, 1)
         ok = sy.wait_warp(B_S_FULL + b, (uses[b]++) & 1u) && sy.wait_warp(B_RING + st, (fill / S) & 1u);
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t v[2][32];
-        const uint32_t ta = tmem + lane_bits + (uint32_t)(b * 128 + wg * 64);
-        ptx::tmem_ld32(ta, v[0]);
-        ptx::tmem_ld32(ta + 32, v[1]);
-        ptx::tmem_wait_ld(v[0]);
-        ptx::tmem_wait_ld(v[1]);
+        uint32_t v[2][2][32];                       // [key sub-tile][column chunk]
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+          const uint32_t ta = tmem + lane_bits + (uint32_t)(b * 256 + kt * 128 + wg * 64);
+          ptx::tmem_ld32(ta, v[kt][0]);
+          ptx::tmem_ld32(ta + 32, v[kt][1]);
+        }
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+          ptx::tmem_wait_ld(v[kt][0]);
+          ptx::tmem_wait_ld(v[kt][1]);
+        }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(sy.bar(B_S_FREE + b));
         const float* wt = reinterpret_cast<const float*>(smem + C::kOffW + st * C::kWBytes);
         const int i0 = (u.g0 + s) * R + wg * RW;    // first query row of this warpgroup's columns
-        float acc[RW];
+        float acc[2][RW];
 #pragma unroll
         for (int rl = 0; rl < RW; ++rl) {
-          float a = 0.f;
+          float a0 = 0.f, a1 = 0.f;
 #pragma unroll
           for (int hh = 0; hh < H; ++hh) {
             const int c = rl * H + hh;
-            a = fmaf(wt[(wg * RW + rl) * H + hh], fmaxf(__uint_as_float(v[c >> 5][c & 31]), 0.f), a);
+            const float wv = wt[(wg * RW + rl) * H + hh];
+            a0 = fmaf(wv, fmaxf(__uint_as_float(v[0][c >> 5][c & 31]), 0.f), a0);
+            a1 = fmaf(wv, fmaxf(__uint_as_float(v[1][c >> 5][c & 31]), 0.f), a1);
           }
-          acc[rl] = a;
+          acc[0][rl] = a0;
+          acc[1][rl] = a1;
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(sy.bar(B_RING + C::kStages + st));
 #pragma unroll
-        for (int rl = 0; rl < RW; ++rl) {
-          const int i = i0 + rl;
-          if (live && i < u.len_q && (int64_t)j <= (int64_t)i + u.shift)
-            p.scores[(int64_t)(u.off_o + i) * p.score_row + j] = acc[rl];
+        for (int kt = 0; kt < 2; ++kt) {
+          const int jr = kt * 128 + row;               // key within the unit
+          const int j = u.k0 + jr;
+#pragma unroll
+          for (int rl = 0; rl < RW; ++rl) {
+            const int i = i0 + rl;
+            if (jr < u.n_keys && i < u.len_q && (int64_t)j <= (int64_t)i + u.shift)
+              p.scores[(int64_t)(u.off_o + i) * p.score_row + j] = acc[kt][rl];
+          }
         }
       }
       if (!ok) break;
@@ -296,7 +317,7 @@ __global__ void __launch_bounds__(kThreadsIx, 1)
   ptx::tc_fence_after();
   if (warp == kAllocWarp) {
     __syncwarp();
-    ptx::tmem_dealloc(tmem, 256);
+    ptx::tmem_dealloc(tmem, 512);
   }
 }
 

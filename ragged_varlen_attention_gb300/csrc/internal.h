@@ -198,6 +198,7 @@ struct IndexerParams {
 cudaError_t launch_indexer_scores_simt(const IndexerParams& p, thd_dtype_t dtype, int num_sms, cudaStream_t stream);
 cudaError_t launch_indexer_topk(const IndexerParams& p, int num_sms, cudaStream_t stream);
 constexpr int kIndexerRowsPerUnit = 128;
+constexpr int kIndexerKeysPerUnit = 256;   // keys of a tensor-core score unit
 constexpr int kIndexerMaxTopk = 2048;
 
 // index of query row i (of sequence b) and head h in BwdParams::ld
