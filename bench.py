@@ -237,27 +237,37 @@ def oracle_sample_time(batch, budget_s: float, max_rows: int | None = None):
 
 
 def run_reference(args, batch):
-    """CPU oracle timed on the host cores over a bounded sample per step."""
+    """CPU oracle timed on the host cores over a bounded sample per step (the
+    forward, or with --bwd / --indexer the backward or indexer oracle)."""
     dist, rank, world, local = dist_setup(args.gpus)
     if rank != 0:
         return
     cores = os.cpu_count()
     per_step_budget = args.ref_step_seconds
+    if args.indexer:
+        sample = oracle_indexer_sample_time
+    elif args.bwd:
+        sample = oracle_bwd_sample_time
+    else:
+        sample = oracle_sample_time
     for _ in range(args.warmup):
-        oracle_sample_time(batch, per_step_budget / 4)
+        sample(batch, per_step_budget / 4)
     times, flops = [], []
     desc = ""
     for _ in range(args.steps):
-        s, f, desc = oracle_sample_time(batch, per_step_budget)
+        s, f, desc = sample(batch, per_step_budget)
         times.append(s)
         flops.append(f)
     total_s, total_f = sum(times), sum(flops)
     value = total_f / total_s / 1e12
+    metric = IDX_METRIC if args.indexer else (BWD_METRIC if args.bwd else METRIC)
+    config = ({"workload": IDX_DESC, "name": "indexer_cp", "pass": "indexer"} if args.indexer
+              else {**config_block(args, batch), **({"pass": "backward"} if args.bwd else {})})
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_block(args, batch),
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"per step: {desc}; budget {per_step_budget:.1f} s"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -300,7 +310,10 @@ def main():
 
     from ragged_varlen_attention_gb300 import workloads as wl
     if args.indexer:
-        bench_indexer(args)
+        if args.impl == "reference":
+            run_reference(args, wl.indexer_cp())
+        else:
+            bench_indexer(args)
         return
     batch = wl.make(args.workload)
     if args.window_left is not None:
@@ -720,7 +733,7 @@ def oracle_indexer_sample_time(b, budget_s: float):
     c = int(b.q_causal_offset[0])
     secs, flops, rows_done, r0 = 0.0, 0, 0, 0
     while secs < budget_s and r0 < q64.shape[0]:
-        r1 = min(q64.shape[0], r0 + 8)
+        r1 = min(q64.shape[0], r0 + 2)
         kmax = min(k64.shape[0], r1 - 1 + c + 1)
         t0 = time.perf_counter()
         sc = indexer_scores_one(q64[r0:r1], k64[:kmax], w64[r0:r1])
@@ -730,7 +743,7 @@ def oracle_indexer_sample_time(b, budget_s: float):
         flops += 2 * b.heads * b.d * int(vis.sum())
         rows_done += r1 - r0
         r0 = r1
-    return secs, flops, f"{rows_done} query rows of document 0 (8 rows per oracle call, each against its visible keys), float64 numpy"
+    return secs, flops, f"{rows_done} query rows of document 0 (2 rows per oracle call, each against its visible keys), float64 numpy"
 
 
 def bench_indexer(args):
