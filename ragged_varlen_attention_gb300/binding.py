@@ -149,7 +149,8 @@ def load_library():
 
 
 class ThdAttnPlan:
-    """Owns a ``thd_attn_plan_t``; frees it when collected."""
+    """Owns a ``thd_attn_plan_t`` (forward, backward or indexer plan); frees it when
+    collected."""
 
     def __init__(self, handle: int, workspace_bytes: int, desc: ThdAttnDesc):
         self.handle = handle
@@ -272,16 +273,7 @@ def indexer_plan_for_tensors(q_i, k_i, w, idx_out, batch: int, topk: int, max_se
     st = lib.thd_indexer_plan(ctypes.byref(handle), ctypes.byref(d), ctypes.byref(ws))
     if st != 0:
         raise ThdAttnError(st, "thd_indexer_plan")
-    plan = ThdAttnPlan.__new__(ThdAttnPlan)
-    plan.handle, plan.workspace_bytes, plan.desc = handle.value, ws.value, d
-    plan.kernel = lib.thd_attn_plan_kernel(handle.value)
-    a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-    lib.thd_attn_plan_geometry(handle.value, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
-    plan.rows_per_unit, plan.keys_per_tile, plan.max_pairs = a.value, b.value, c.value
-    offs = (ctypes.c_int64 * 4)()
-    lib.thd_attn_plan_workspace_layout(handle.value, offs)
-    plan.workspace_layout = tuple(int(x) for x in offs)
-    return plan
+    return ThdAttnPlan(handle.value, ws.value, d)
 
 
 def _ptr(t):
