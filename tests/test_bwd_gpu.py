@@ -51,9 +51,11 @@ def _dout(batch: wl.ThdBatch, seed: int) -> torch.Tensor:
 
 
 def run_bwd(batch: wl.ThdBatch, kernel=bd.KERNEL_AUTO, gaps=(0,) * 8, seed=0, flags=0, device="cuda",
-            device_mask=None):
+            device_mask=None, element_mult=None):
     """Forward outputs from the oracle, then the backward through the C ABI
-    (``device_mask`` replaces the mask array passed to the device)."""
+    (``device_mask`` replaces the mask array passed to the device; with
+    ``element_mult`` the offsets go in element units: row x token stride of the
+    primal tensor, divided by the multiplier)."""
     o_ref, s_ref, written = oracle_on_batch(batch)
     o_host = batch.o_init().clone()
     o_host[torch.from_numpy(written)] = torch.from_numpy(o_ref[written]).to(batch.torch_dtype)
@@ -72,13 +74,25 @@ def run_bwd(batch: wl.ThdBatch, kernel=bd.KERNEL_AUTO, gaps=(0,) * 8, seed=0, fl
     (dq, dqb), (dk, dkb), (dv, dvb) = grads
     stats = stats_host.to(device)
     ints = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
-    offs = [ints(x) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)]
+    row_offs = (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)
+    mult = 0
+    if element_mult is not None:
+        flags |= bd.FLAG_ELEMENT_OFFSETS
+        mult = element_mult
+        strides = (q.stride(0), k.stride(0), v.stride(0), o.stride(0), batch.stats_strides[0])
+        conv = []
+        for off, sd in zip(row_offs, strides):
+            e = off.astype(np.int64) * sd
+            assert (e % max(1, mult) == 0).all()
+            conv.append(e // max(1, mult))
+        row_offs = conv
+    offs = [ints(x) for x in row_offs]
     mask = torch.from_numpy(np.ascontiguousarray(batch.mask_type if device_mask is None else device_mask,
                                                  dtype=np.int8)).to(device)
     qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
     win = None if batch.window_left is None else ints(batch.window_left)
     plan = bd.plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch.batch, batch.cap_s, batch.stats_layout,
-                                   batch.softmax_scale, kernel, flags)
+                                   batch.softmax_scale, kernel, flags, mult)
     ws = bd.alloc_workspace(plan, device)
     bd.thd_attn_bwd(plan, q, k, v, o, d_o, stats, dq, dk, dv, ints(batch.cu_seqlens_q),
                     ints(batch.cu_seqlens_kv), *offs, mask, qco, win, ws)
@@ -207,3 +221,16 @@ def test_bwd_invalid_sequence_flagged_and_untouched():
                         ("dvb", batch.off_v[1], batch.lens_k()[1])):
         raw = res[key].view(torch.uint8).numpy().reshape(res[key].shape[0], -1)
         assert (raw[off:off + n] == SENTINEL).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("mult", [0, 2])
+def test_bwd_element_offsets(kernel, mult):
+    """Element-unit offsets (row x the primal tensor's token stride, over the
+    multiplier) give the same gradients as row offsets; gradient views keep their
+    own strides (token gaps)."""
+    batch = wl.random_pack(7400 + mult, batch=4, max_len=300, h_q=4, h_kv=2, d=64, dtype="bf16",
+                           stats_layout=wl.STATS_TOKEN_MAJOR)
+    res = run_bwd(batch, kernel=kernel, gaps=(1, 0, 1, 0, 2, 1, 0, 2), seed=17, element_mult=mult)
+    assert res["status"] == 0
+    check_bwd(batch, res)

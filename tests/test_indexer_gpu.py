@@ -146,3 +146,12 @@ def test_indexer_key_length_over_bound_is_flagged():
     b = int(np.argmax(lk))
     o, n = int(batch.off_out[b]), int(batch.lens_q()[b])
     assert (res["idx"][o:o + n] == SENT).all()
+
+
+def test_indexer_128_heads_simt():
+    """H = 128 (more heads than a tensor-core column group holds) runs on the SIMT
+    scores with the same selection."""
+    batch = wl.indexer_random_pack(8500, batch=3, max_len=400, heads=128, d=128, topk=32, zero_q_rows=2)
+    res = run_indexer(batch)
+    assert res["status"] == 0 and res["plan"].kernel == bd.KERNEL_SIMT
+    check_indexer(batch, res, exact_rows=True)
