@@ -234,3 +234,160 @@ def test_bwd_element_offsets(kernel, mult):
     res = run_bwd(batch, kernel=kernel, gaps=(1, 0, 1, 0, 2, 1, 0, 2), seed=17, element_mult=mult)
     assert res["status"] == 0
     check_bwd(batch, res)
+
+
+def _bwd_after_fwd(batch: wl.ThdBatch, kernel=bd.KERNEL_AUTO, seed=21, device="cuda"):
+    # the forward always takes the automatic choice, so that two backward kernels
+    # compared with each other read the same O and Stats
+    """The benchmark's launch configuration: packed views, O and Stats from this
+    library's forward on the same inputs (they are inputs of the backward, not of
+    the oracle, which recomputes P from Q and K), dO seeded with NaN pad rows,
+    gradient buffers filled with the byte sentinel."""
+    ints = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(device)
+    q, k, v = (t.to(device) for t in (batch.q, batch.k, batch.v))
+    o = batch.o_init().to(device)
+    stats = torch.zeros((batch.stats_numel,), dtype=torch.float32, device=device)
+    d_o = _dout(batch, seed).to(device)
+    cu_q, cu_k = ints(batch.cu_seqlens_q), ints(batch.cu_seqlens_kv)
+    offs = [ints(x) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o, batch.off_s)]
+    mask = ints(batch.mask_type, np.int8)
+    qco = None if batch.q_causal_offset is None else ints(batch.q_causal_offset)
+    fplan = bd.plan_for_tensors(q, k, v, o, batch.batch, batch.cap_s, batch.stats_layout, batch.softmax_scale)
+    fws = bd.alloc_workspace(fplan, device)
+    bd.thd_attn_fwd(fplan, q, k, v, o, stats, cu_q, cu_k, *offs, mask, qco, fws)
+    assert bd.thd_attn_read_status(fplan, fws) == 0
+    grads = [torch.empty_like(t) for t in (q, k, v)]
+    for g in grads:
+        g.view(torch.uint8).fill_(SENTINEL)
+    dq, dk, dv = grads
+    plan = bd.plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch.batch, batch.cap_s, batch.stats_layout,
+                                   batch.softmax_scale, kernel, 0)
+    ws = bd.alloc_workspace(plan, device)
+    bd.thd_attn_bwd(plan, q, k, v, o, d_o, stats, dq, dk, dv, cu_q, cu_k, *offs, mask, qco, None, ws)
+    status = bd.thd_attn_read_status(plan, ws)
+    torch.cuda.synchronize()
+    return dict(dq=dq.cpu(), dk=dk.cpu(), dv=dv.cpu(), d_o=d_o.cpu(), status=status, plan=plan)
+
+
+def _check_group(batch: wl.ThdBatch, res, b: int, g: int):
+    """Every row of sequence ``b``'s dQ (query heads of kv group ``g``) and of its
+    dK / dV at kv head ``g`` against the oracle, one query head at a time."""
+    from oracle.thd_attention import causal_shift
+    lq, lk = int(batch.lens_q()[b]), int(batch.lens_k()[b])
+    qs, ks, vs, os_ = (int(x[b]) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o))
+    shift = causal_shift(int(batch.mask_type[b]), lq, lk,
+                         None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+    scale = batch.softmax_scale if batch.softmax_scale is not None else 1.0 / np.sqrt(batch.d)
+    group = batch.h_q // batch.h_kv
+    f64 = lambda t: t.to(torch.float64).numpy()
+    kb, vb = f64(batch.k[ks:ks + lk, g]), f64(batch.v[vs:vs + lk, g])
+    acc_k, acc_v = np.zeros_like(kb), np.zeros_like(vb)
+    tol = TOL[batch.dtype]
+
+    def close(name, got, ref):
+        assert np.isfinite(got).all(), f"non-finite {name}"
+        err = float(np.max(np.abs(got - ref), initial=0.0)) / max(1.0, float(np.max(np.abs(ref), initial=0.0)))
+        assert err <= tol, f"seq {b} group {g} {name}: normalised error {err} > {tol}"
+
+    for h in range(g * group, (g + 1) * group):
+        gq, gk, gv = ob.attention_one_head_bwd(f64(batch.q[qs:qs + lq, h]), kb, vb,
+                                               f64(res["d_o"][os_:os_ + lq, h]), scale, shift)
+        close(f"dq head {h}", f64(res["dq"][qs:qs + lq, h]), gq)
+        acc_k += gk
+        acc_v += gv
+    close("dk", f64(res["dk"][ks:ks + lk, g]), acc_k)
+    close("dv", f64(res["dv"][vs:vs + lk, g]), acc_v)
+
+
+def _written_rows(offs, lens, cap):
+    w = np.zeros(cap, dtype=bool)
+    for o, n in zip(offs, lens):
+        w[int(o):int(o) + int(n)] = True
+    return w
+
+
+def _check_dq_rows(batch: wl.ThdBatch, res, b: int, rows, heads):
+    """dQ of single query rows: row i's gradient depends on row i alone, so a
+    one-row problem with the row's own causal shift gives it exactly."""
+    from oracle.thd_attention import causal_shift
+    lq, lk = int(batch.lens_q()[b]), int(batch.lens_k()[b])
+    qs, ks, vs, os_ = (int(x[b]) for x in (batch.off_q, batch.off_k, batch.off_v, batch.off_o))
+    shift = causal_shift(int(batch.mask_type[b]), lq, lk,
+                         None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+    scale = batch.softmax_scale if batch.softmax_scale is not None else 1.0 / np.sqrt(batch.d)
+    group = batch.h_q // batch.h_kv
+    f64 = lambda t: t.to(torch.float64).numpy()
+    tol = TOL[batch.dtype]
+    for h in heads:
+        g = h // group
+        kb, vb = f64(batch.k[ks:ks + lk, g]), f64(batch.v[vs:vs + lk, g])
+        for r in rows:
+            gq, _, _ = ob.attention_one_head_bwd(f64(batch.q[qs + r:qs + r + 1, h]), kb, vb,
+                                                 f64(res["d_o"][os_ + r:os_ + r + 1, h]), scale,
+                                                 None if shift is None else shift + r)
+            got = f64(res["dq"][qs + r:qs + r + 1, h])
+            err = float(np.max(np.abs(got - gq))) / max(1.0, float(np.max(np.abs(gq))))
+            assert err <= tol, f"seq {b} row {r} head {h}: dq normalised error {err} > {tol}"
+
+
+def _check_dv_sums(batch: wl.ThdBatch, res, b: int):
+    """An identity of the softmax gradient that holds at any size, per kv head g:
+    sum_j dV_j = sum of dO_i over the group's heads and the live rows (every live
+    row of P sums to one), so it checks the Stats each key tile reads. Tolerance
+    2e-2 of max(1, |sum dO|): 16-bit rounding of the stored dV moves the sum by at
+    most 2^-8 of sum_i |dO_i| and by far less in practice, a misread Stats row by
+    a factor. (The companion identity sum_j dK_j = 0 has no usable bound here: the
+    16-bit dS rounding is not small against the cancelling sum.)"""
+    from oracle.thd_attention import causal_shift
+    lq, lk = int(batch.lens_q()[b]), int(batch.lens_k()[b])
+    vs, os_ = int(batch.off_v[b]), int(batch.off_o[b])
+    shift = causal_shift(int(batch.mask_type[b]), lq, lk,
+                         None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+    n_vis = np.full(lq, lk) if shift is None else np.clip(np.arange(lq) + shift + 1, 0, lk)
+    live = torch.from_numpy(n_vis > 0)
+    group = batch.h_q // batch.h_kv
+    d_o = res["d_o"][os_:os_ + lq][live].to(torch.float64)                      # [live, h_q, d]
+    want = d_o.view(-1, batch.h_kv, group, batch.d).sum(dim=(0, 2))            # [h_kv, d]
+    got = res["dv"][vs:vs + lk].to(torch.float64).sum(dim=0)
+    err = float((got - want).abs().max()) / max(1.0, float(want.abs().max()))
+    assert err <= 2e-2, f"seq {b}: sum of dV rows off by {err}"
+
+
+@pytest.mark.parametrize("name", ["cp_chunks", "mixed_gqa"])
+def test_bwd_full_size_sampled(name):
+    """Full-size workloads in the benchmark's launch configuration. cp_chunks: dQ of
+    sampled rows of both documents at three heads against the oracle (one whole
+    65536-key head costs the oracle about a minute, so dK and dV are checked through
+    the dV row-sum identity and against the SIMT kernel); mixed_gqa: every row of
+    the longest sequence and two others at sampled kv groups. Both: the identity on
+    every sequence, pad rows untouched, every row against the SIMT backward."""
+    batch = wl.make(name)
+    res = _bwd_after_fwd(batch)
+    assert res["status"] == 0
+    assert res["plan"].kernel == bd.KERNEL_TCGEN05
+    lq, lk = batch.lens_q(), batch.lens_k()
+    rng = np.random.default_rng(3)
+    if name == "cp_chunks":
+        for b in range(batch.batch):
+            L = int(lq[b])
+            rows = sorted({0, 1, 127, 128, 129, 255, 256, L - 2, L - 1, *rng.integers(0, L, size=3).tolist()})
+            _check_dq_rows(batch, res, b, rows, heads=(0, batch.h_q // 2 - 1, batch.h_q - 1))
+    else:
+        longest = int(np.argmax(lq))
+        others = [int(x) for x in rng.choice(np.nonzero(lq > 0)[0], size=3, replace=False) if x != longest][:2]
+        pairs = [(longest, 0), (longest, batch.h_kv - 1)] + [(b, int(rng.integers(batch.h_kv))) for b in others]
+        for b, g in pairs:
+            _check_group(batch, res, b, g)
+    for b in range(batch.batch):
+        _check_dv_sums(batch, res, b)
+    for key, offs, lens in (("dq", batch.off_q, lq), ("dk", batch.off_k, lk), ("dv", batch.off_v, lk)):
+        raw = res[key].view(torch.uint8).numpy().reshape(res[key].shape[0], -1)
+        w = _written_rows(offs, lens, raw.shape[0])
+        assert (raw[~w] == SENTINEL).all(), f"a pad row of {key} was written"
+    alt = _bwd_after_fwd(batch, kernel=bd.KERNEL_SIMT)
+    assert alt["status"] == 0
+    for key, offs, lens in (("dq", batch.off_q, lq), ("dk", batch.off_k, lk), ("dv", batch.off_v, lk)):
+        w = torch.from_numpy(_written_rows(offs, lens, res[key].shape[0]))
+        a, r = res[key][w].float(), alt[key][w].float()
+        err = float((a - r).abs().max()) / max(1.0, float(r.abs().max()))
+        assert err <= 2 * TOL[batch.dtype], f"{key}: tcgen05 vs SIMT normalised error {err}"

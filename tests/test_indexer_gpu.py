@@ -51,15 +51,51 @@ def run_indexer(batch: wl.IndexerBatch, kernel=bd.KERNEL_AUTO, max_seqlen_k=0, d
     return dict(idx=idx.cpu().numpy(), scores=sc.cpu().numpy(), status=status, plan=plan)
 
 
+def _check_row(tag, row, srow, s_vis, ref_row, topk, exact=False):
+    """One output row against the oracle's scores of the row's visible keys
+    (``s_vis``, float64) and the oracle's selection ``ref_row``."""
+    n_vis = s_vis.shape[0]
+    n_out = min(topk, n_vis)
+    assert (row[:n_out] >= 0).all() and (row[n_out:] == -1).all(), f"{tag}: count"
+    sel = row[:n_out]
+    assert len(set(sel.tolist())) == n_out and (sel < n_vis).all(), f"{tag}: bad index"
+    assert np.isnan(srow[n_out:]).all()
+    if n_out == 0:
+        return
+    tau = 1e-3 * (1.0 + float(np.abs(s_vis).max()))
+    kth = float(s_vis[ref_row[n_out - 1]])
+    assert (s_vis[sel] >= kth - tau).all(), f"{tag}: a selected key scores below the k-th"
+    must = np.nonzero(s_vis > kth + tau)[0]
+    assert set(must.tolist()) <= set(sel.tolist()), f"{tag}: a clearly better key is missing"
+    assert np.abs(srow[:n_out] - s_vis[sel]).max() <= tau
+    assert (np.diff(srow[:n_out]) <= 0).all(), f"{tag}: not in descending order"
+    if exact:
+        assert list(sel) == list(ref_row[:n_out]), f"{tag}: tie order"
+
+
+def _n_visible(batch, b, i):
+    lq, lk = int(batch.lens_q()[b]), int(batch.lens_k()[b])
+    shift = causal_shift(int(batch.mask_type[b]), lq, lk,
+                         None if batch.q_causal_offset is None else batch.q_causal_offset[b])
+    return lk if shift is None else max(0, min(lk, i + shift + 1))
+
+
+def _check_untouched(batch, res):
+    written = np.zeros(batch.cap_out, dtype=bool)
+    for b in range(batch.batch):
+        written[int(batch.off_out[b]):int(batch.off_out[b]) + int(batch.lens_q()[b])] = True
+    assert (res["idx"][~written] == SENT).all(), "an output row outside the sequences was written"
+    assert (res["scores"][~written] == -123.0).all()
+
+
 def check_indexer(batch: wl.IndexerBatch, res, exact_rows=False):
     init = np.full((batch.cap_out, batch.topk), SENT, dtype=np.int64)
-    ref_idx, ref_sel, written = ix.indexer_topk(
+    ref_idx, _, written = ix.indexer_topk(
         batch.q.to(torch.float64).numpy(), batch.k.to(torch.float64).numpy(), batch.w.to(torch.float64).numpy(),
         batch.cu_seqlens_q, batch.cu_seqlens_kv, batch.off_q, batch.off_k, batch.off_out, batch.mask_type,
         batch.q_causal_offset, batch.topk, init)
-    got, got_s = res["idx"], res["scores"]
-    assert (got[~written] == SENT).all(), "an output row outside the sequences was written"
-    assert (got_s[~written] == -123.0).all()
+    assert (res["idx"][~written] == SENT).all(), "an output row outside the sequences was written"
+    assert (res["scores"][~written] == -123.0).all()
     lq, lk = batch.lens_q(), batch.lens_k()
     q64, k64, w64 = (t.to(torch.float64).numpy() for t in (batch.q, batch.k, batch.w))
     for b in range(batch.batch):
@@ -67,28 +103,10 @@ def check_indexer(batch: wl.IndexerBatch, res, exact_rows=False):
             continue
         qs, ks, os_ = int(batch.off_q[b]), int(batch.off_k[b]), int(batch.off_out[b])
         S = ix.indexer_scores_one(q64[qs:qs + lq[b]], k64[ks:ks + lk[b]], w64[qs:qs + lq[b]])
-        shift = causal_shift(int(batch.mask_type[b]), int(lq[b]), int(lk[b]),
-                             None if batch.q_causal_offset is None else batch.q_causal_offset[b])
         for i in range(int(lq[b])):
-            n_vis = int(lk[b]) if shift is None else max(0, min(int(lk[b]), i + shift + 1))
-            row, srow = got[os_ + i], got_s[os_ + i]
-            n_out = min(batch.topk, n_vis)
-            assert (row[:n_out] >= 0).all() and (row[n_out:] == -1).all(), f"seq {b} row {i}: count"
-            sel = row[:n_out]
-            assert len(set(sel.tolist())) == n_out and (sel < n_vis).all(), f"seq {b} row {i}: bad index"
-            assert np.isnan(srow[n_out:]).all()
-            if n_out == 0:
-                continue
-            vis_scores = S[i, :n_vis]
-            tau = 1e-3 * (1.0 + float(np.abs(vis_scores).max()))
-            kth = float(ref_sel[os_ + i, n_out - 1])
-            assert (S[i, sel] >= kth - tau).all(), f"seq {b} row {i}: a selected key scores below the k-th"
-            must = np.nonzero(vis_scores > kth + tau)[0]
-            assert set(must.tolist()) <= set(sel.tolist()), f"seq {b} row {i}: a clearly better key is missing"
-            assert np.abs(srow[:n_out] - S[i, sel]).max() <= tau
-            assert (np.diff(srow[:n_out]) <= 0).all(), f"seq {b} row {i}: not in descending order"
-            if exact_rows and not np.any(q64[qs + i]):
-                assert list(sel) == list(ref_idx[os_ + i, :n_out]), f"seq {b} row {i}: tie order"
+            n_vis = _n_visible(batch, b, i)
+            _check_row(f"seq {b} row {i}", res["idx"][os_ + i], res["scores"][os_ + i], S[i, :n_vis],
+                       ref_idx[os_ + i], batch.topk, exact=exact_rows and not np.any(q64[qs + i]))
 
 
 @pytest.mark.parametrize("kernel", [bd.KERNEL_AUTO, bd.KERNEL_SIMT])
@@ -155,3 +173,29 @@ def test_indexer_128_heads_simt():
     res = run_indexer(batch)
     assert res["status"] == 0 and res["plan"].kernel == bd.KERNEL_SIMT
     check_indexer(batch, res, exact_rows=True)
+
+
+def test_indexer_full_size_sampled():
+    """The benchmark's workload in its launch configuration (two 65536-key
+    documents, 4096-row chunks, H = 64, d = 128, k = 2048): sampled rows of both
+    documents against the oracle, which scores each row on its own (rows are
+    independent), and every row outside the sequences untouched."""
+    batch = wl.indexer_cp()
+    res = run_indexer(batch, max_seqlen_k=int(batch.lens_k().max()))
+    assert res["status"] == 0 and res["plan"].kernel == bd.KERNEL_TCGEN05
+    _check_untouched(batch, res)
+    rng = np.random.default_rng(5)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    for b in range(batch.batch):
+        L, lk = int(batch.lens_q()[b]), int(batch.lens_k()[b])
+        qs, ks, os_ = int(batch.off_q[b]), int(batch.off_k[b]), int(batch.off_out[b])
+        kb = f64(batch.k[ks:ks + lk])
+        rows = sorted({0, 1, 127, 128, 129, L - 2, L - 1, *rng.integers(0, L, size=4).tolist()})
+        for i in rows:
+            s_row = ix.indexer_scores_one(f64(batch.q[qs + i:qs + i + 1]), kb, f64(batch.w[qs + i:qs + i + 1]))
+            n_vis = _n_visible(batch, b, i)
+            vis = np.zeros((1, lk), dtype=bool)
+            vis[0, :n_vis] = True
+            ref_row = ix.select_topk(s_row, vis, batch.topk)[0]
+            _check_row(f"doc {b} row {i}", res["idx"][os_ + i], res["scores"][os_ + i], s_row[0, :n_vis],
+                       ref_row, batch.topk)
