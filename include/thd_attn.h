@@ -1,6 +1,7 @@
 /*
  * thd_attn.h -- C ABI of the GB300 (sm_103a) packed-THD attention library
- * (forward, and its backward at the end of this file).
+ * (forward; its backward and the sparse-attention indexer top-k at the end of
+ * this file).
  *
  * Operation (scaled-dot-product attention forward with log-sum-exp Stats over a
  * packed, ragged "THD" batch):
@@ -89,7 +90,7 @@ enum {
   THD_DEV_BAD_LENGTH = 1u << 0,     /* cu_seqlens not non-decreasing for some b */
   THD_DEV_BAD_OFFSET = 1u << 1,     /* off[b] < 0 or off[b] + len > cap_rows for some tensor */
   THD_DEV_BAD_MASK = 1u << 2,       /* mask_type[b] not in {0, 1, 2} */
-  THD_DEV_TILE_OVERFLOW = 1u << 3,  /* more query tiles than the plan's capacity (no work done) */
+  THD_DEV_TILE_OVERFLOW = 1u << 3,  /* more work units than the plan's capacity (no work done) */
   THD_DEV_WAIT_TIMEOUT = 1u << 4    /* a bounded in-kernel wait gave up (kernel returned early) */
 };
 
@@ -183,8 +184,10 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
                                  const int32_t* q_causal_offset, const int32_t* window_left,
                                  void* workspace, void* stream);
 
-/* Copy the device status word of the last fwd on this workspace to *host_out and
- * synchronise `stream`. This is the only call that waits on the device. */
+/* Copy the device status word of the last call on this workspace (fwd, bwd or
+ * indexer top-k with this plan; the OR of both schedules' words where a call
+ * builds two) to *host_out and synchronise `stream`. This is the only call that
+ * waits on the device. */
 thd_status_t thd_attn_read_status(thd_attn_plan_t plan, const void* workspace,
                                   uint32_t* host_out, void* stream);
 
@@ -198,8 +201,9 @@ void thd_attn_plan_geometry(thd_attn_plan_t plan, int32_t* rows_per_unit,
 
 /* Byte offsets, inside the workspace, of its first four regions: [0] header words
  * (tile counter, status, entry count, tile count, first entry of each cost group,
- * split count), [1] per-sequence metadata (8 int32 per sequence: len_q, len_k,
- * off_q, off_k, off_v, off_o, off_s, shift), [2] per-sequence first pair index
+ * split count), [1] per-sequence metadata (12 int32 per sequence: len_q, len_k,
+ * off_q, off_k, off_v, off_o, off_s, shift, window lower shift, 3 unused), [2]
+ * per-sequence first pair index
  * (int32 [B+1]), [3] the scheduled entry list (int32 {b, first query row, split,
  * partial slot} per entry, longest first). For inspection only. */
 void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]);
@@ -342,8 +346,11 @@ typedef struct {
   uint32_t flags;                 /* none defined; must be 0 */
 } thd_indexer_desc_t;
 
-/* Validate and size (host only). The workspace holds the schedule and a float32
- * score row of max_seqlen_k entries per output row. */
+/* Validate and size (host only). The workspace holds the schedules and a float32
+ * score row of max_seqlen_k entries (rounded up to 128) per output row. Segments
+ * may share key rows (the zigzag query chunks of one document under context
+ * parallelism all read its key prefix): the key-axis schedule is sized per
+ * segment from max_seqlen_k, not from cap_rows_k. */
 thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* desc, size_t* workspace_bytes);
 
 /* Enqueue the indexer top-k (asynchronous, no allocation, no device->host read).

@@ -34,6 +34,12 @@ float scale_of(const thd_attn_desc_t& d) {
   return std::isnan(d.softmax_scale) ? 1.0f / std::sqrt((float)d.d) : d.softmax_scale;
 }
 
+// an indexer plan whose calls build a key-axis schedule (tensor-core scores)
+bool indexer_uses_key_axis(const thd_attn_plan_s* plan) {
+  return plan->is_indexer && plan->kernel == THD_KERNEL_TCGEN05 && plan->idesc.cap_rows_q > 0 &&
+         plan->idesc.cap_rows_k > 0;
+}
+
 bool tc_applicable(const thd_attn_desc_t& d, float scale) {
   if (!thd::tc_kernel_available()) return false;
   if (!(scale > 0.f)) return false;  // the softmax takes the row max of unscaled scores
@@ -361,9 +367,11 @@ thd_status_t thd_attn_read_status(thd_attn_plan_t plan, const void* workspace, u
   uint32_t words[2] = {0u, 0u};
   if (cudaMemcpyAsync(&words[0], src, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return THD_ERR_CUDA;
-  if (plan->is_bwd) {
-    // the key-axis schedule of the backward keeps its own status word
-    const char* src_k = static_cast<const char*>(workspace) + plan->ws_off_b[0] + 4 * thd::kHdrStatus;
+  if (plan->is_bwd || indexer_uses_key_axis(plan)) {
+    // the key-axis schedules of the backward and of the tensor-core indexer keep
+    // their own status word
+    const int64_t hdr = plan->is_bwd ? plan->ws_off_b[0] : plan->ws_off_b[1];
+    const char* src_k = static_cast<const char*>(workspace) + hdr + 4 * thd::kHdrStatus;
     if (cudaMemcpyAsync(&words[1], src_k, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
       return THD_ERR_CUDA;
   }
@@ -617,8 +625,15 @@ thd_status_t thd_indexer_plan(thd_attn_plan_t* out, const thd_indexer_desc_t* de
   p->score_row = align_up(max_len > 0 ? max_len : 1, 128);
   const int64_t max_pairs = (int64_t)d.batch + (d.cap_rows_out + p->rows_per_unit - 1) / p->rows_per_unit + 1;
   p->max_pairs = (int32_t)max_pairs;
-  // key-axis units (tensor-core scores): non-overlapping key rows bound them
-  const int64_t max_k = (int64_t)d.batch + (d.cap_rows_k + thd::kIndexerKeysPerUnit - 1) / thd::kIndexerKeysPerUnit + 1;
+  // key-axis units (tensor-core scores): sequences may share key rows (the query
+  // chunks of one document under context parallelism all read its key prefix), so
+  // the bound is per sequence: len_k <= max_len (checked on the device)
+  const int64_t max_k =
+      (int64_t)d.batch * ((max_len + thd::kIndexerKeysPerUnit - 1) / thd::kIndexerKeysPerUnit) + 1;
+  if (max_k >= (int64_t(1) << 31) || max_pairs >= (int64_t(1) << 31)) {
+    delete p;
+    return THD_ERR_UNSUPPORTED;
+  }
   p->max_pairs_k = (int32_t)max_k;
   int64_t off = 0;
   p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
@@ -648,6 +663,14 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
   if ((!q_i || !w) && d.cap_rows_q > 0) return THD_ERR_INVALID_ARG;
   if (!k_i && d.cap_rows_k > 0) return THD_ERR_INVALID_ARG;
   if (!idx_out && d.cap_rows_out > 0) return THD_ERR_INVALID_ARG;
+  // every check that can fail comes before the first launch, so that a status read
+  // after a successful call always sees headers this call's setup kernels wrote
+  const bool use_tc = indexer_uses_key_axis(plan);
+  if (use_tc) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q_i) | reinterpret_cast<uintptr_t>(k_i) |
+                        reinterpret_cast<uintptr_t>(w);
+    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
+  }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   char* ws = static_cast<char*>(workspace);
   const int num_sms = num_sms_of_current_device();
@@ -678,12 +701,6 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
   sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
   sp.splits = nullptr;
   if (thd::launch_setup(sp, stream) != cudaSuccess) return THD_ERR_CUDA;
-  bool use_tc = plan->kernel == THD_KERNEL_TCGEN05 && d.cap_rows_q > 0 && d.cap_rows_k > 0;
-  if (use_tc) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(q_i) | reinterpret_cast<uintptr_t>(k_i) |
-                        reinterpret_cast<uintptr_t>(w);
-    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
-  }
   thd::IndexerParams ip;
   ip.header_k = nullptr;
   ip.counter_k = nullptr;

@@ -358,3 +358,27 @@ def indexer_random_pack(seed: int, *, batch: int = 4, max_len: int = 300, heads:
     qco = np.array([int(rng.integers(-2, int(b_) + 3)) for b_ in lk], dtype=np.int32)
     return IndexerBatch(f"indexer_random_{seed}", dtype, heads, d, topk, _cumsum0(lq), _cumsum0(lk),
                         off_q, off_k, off_o, mask, qco, q, k, w, cap_o)
+
+
+def indexer_zigzag(seed: int = 107, doc_len: int = 4096, cp_size: int = 2, ranks=(0, 1), heads: int = 8,
+                   d: int = 64, topk: int = 64, dtype: str = "bf16") -> IndexerBatch:
+    """Zigzag context-parallel query chunks of one document (Megatron-LM PR #14,
+    the packed-CP indexer paths): the document is cut into 2 * cp_size chunks of
+    doc_len / (2 * cp_size) rows and rank r holds chunks r and 2 * cp_size - 1 - r.
+    Every chunk becomes one THD segment whose queries see the key prefix that ends
+    with the chunk, bottom-right aligned at q_causal_offset = the chunk's first
+    global row. All segments read the SAME key rows (off_k = 0), so the segments'
+    key ranges overlap."""
+    rng = np.random.default_rng(seed)
+    c = doc_len // (2 * cp_size)
+    chunks = [ch for r in ranks for ch in (r, 2 * cp_size - 1 - r)]
+    lq = np.full(len(chunks), c, dtype=np.int64)
+    lk = np.array([(ch + 1) * c for ch in chunks], dtype=np.int64)
+    off_q = _cumsum0(lq)[:-1].astype(np.int32)
+    q = _normal(rng, (int(lq.sum()), heads, d), dtype)
+    k = _normal(rng, (doc_len, d), dtype)
+    w = torch.from_numpy((rng.standard_normal((int(lq.sum()), heads)) / np.sqrt(heads)).astype(np.float32))
+    return IndexerBatch(f"indexer_zigzag_{seed}", dtype, heads, d, topk, _cumsum0(lq), _cumsum0(lk), off_q,
+                        np.zeros(len(chunks), dtype=np.int32), off_q.copy(),
+                        np.full(len(chunks), MASK_BOTTOM_RIGHT, dtype=np.int8),
+                        np.array([ch * c for ch in chunks], dtype=np.int32), q, k, w, int(lq.sum()))

@@ -248,3 +248,17 @@ def test_indexer_plan_validation_and_sizing(lib):
     assert _plan_ix(_ix_desc(heads=2))[2] == bd.KERNEL_SIMT          # H must be 4..64 for tensor cores
     assert _plan_ix(_ix_desc(heads=2, kernel=bd.KERNEL_TCGEN05))[0] == 2
     assert _plan_ix(_ix_desc(d=96))[2] == bd.KERNEL_SIMT
+
+
+def test_indexer_key_schedule_sized_per_segment(lib):
+    """Segments may share key rows (zigzag context-parallel chunks of one document),
+    so the key-axis schedule holds batch x ceil(max_seqlen_k / 256) units (16 bytes
+    each), not a bound derived from cap_rows_k: with the key and output capacities
+    fixed, each extra segment adds at least 16 units of 256 keys at max_seqlen_k =
+    4096."""
+    small = dict(heads=8, d=64, topk=64, cap_rows_q=4096, stride_tok_q=8 * 64, stride_head_q=64,
+                 cap_rows_k=4096, stride_tok_k=64, stride_tok_w=8, cap_rows_out=4096, max_seqlen_k=4096)
+    sizes = [_plan_ix(_ix_desc(batch=b, **small)) for b in (1, 4, 16)]
+    assert all(st == 0 and k == bd.KERNEL_TCGEN05 for st, _, k in sizes)
+    ws = [w for _, w, _ in sizes]
+    assert ws[1] - ws[0] >= 3 * 16 * 16 and ws[2] - ws[1] >= 12 * 16 * 16

@@ -199,3 +199,15 @@ def test_indexer_full_size_sampled():
             ref_row = ix.select_topk(s_row, vis, batch.topk)[0]
             _check_row(f"doc {b} row {i}", res["idx"][os_ + i], res["scores"][os_ + i], s_row[0, :n_vis],
                        ref_row, batch.topk)
+
+
+def test_indexer_zigzag_chunks_share_keys():
+    """Zigzag context-parallel chunks of one 4096-token document (two ranks of
+    cp_size 2, chunks of 1024 rows): four segments read overlapping key prefixes
+    of the same key rows, 40 key units of 256 against 21 if key rows could not be
+    shared -- the key-axis schedule must hold them all."""
+    batch = wl.indexer_zigzag()
+    assert int(np.sum(batch.lens_k())) > batch.k.shape[0]
+    res = run_indexer(batch)
+    assert res["status"] == 0 and res["plan"].kernel == bd.KERNEL_TCGEN05
+    check_indexer(batch, res)
