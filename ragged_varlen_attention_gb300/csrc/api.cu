@@ -489,6 +489,19 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   for (int i = 0; i < 4; ++i)
     if (!grads[i] && plan->g_cap_rows[i] > 0) return THD_ERR_INVALID_ARG;
   if (!stats && d.cap_rows_stats > 0) return THD_ERR_INVALID_ARG;
+  // every check that can fail comes before the first launch
+  // a view with no rows has no TMA descriptor: the SIMT kernels serve that call
+  bool use_tc = plan->kernel == THD_KERNEL_TCGEN05;
+  for (int i = 0; i < 3; ++i)
+    if (d.cap_rows[i] == 0) use_tc = false;
+  if (plan->g_cap_rows[0] == 0) use_tc = false;
+  if (use_tc) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(d_o) |
+                        reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+                        reinterpret_cast<uintptr_t>(dv);
+    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
+  }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   char* ws = static_cast<char*>(workspace);
   const int num_sms = num_sms_of_current_device();
@@ -561,18 +574,6 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   bp.keys_per_unit = thd::kBwdKeysPerUnit;
   bp.has_window = window_left != nullptr ? 1 : 0;
 
-  // a view with no rows has no TMA descriptor: the SIMT kernels serve that call
-  bool use_tc = plan->kernel == THD_KERNEL_TCGEN05;
-  for (int i = 0; i < 3; ++i)
-    if (d.cap_rows[i] == 0) use_tc = false;
-  if (plan->g_cap_rows[0] == 0) use_tc = false;
-  if (use_tc) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(d_o) |
-                        reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
-                        reinterpret_cast<uintptr_t>(dv);
-    if (a % 16 != 0) return THD_ERR_ALIGNMENT;
-  }
   if (thd::launch_bwd_prep(bp, d.dtype, num_sms, stream) != cudaSuccess) return THD_ERR_CUDA;
   const bool prof = plan->prof_events && plan->prof_count < plan->prof_slots;
   if (prof && cudaEventRecord(plan->prof_events[2 * plan->prof_count], stream) != cudaSuccess)
