@@ -11,7 +11,10 @@
   chunk the bottom-right mask with q_causal_offset gives row i the prefix
   0 .. i + c, while the top-left mask gives the chunk-local window 0 .. i
   (Megatron-LM PR #14);
-* selected scores dominate every unselected visible score.
+* selected scores dominate every unselected visible score;
+* the zigzag context-parallel chunks of one document select what the
+  full-document causal indexer selects for the same rows (the pages' exact
+  index-parity check).
 
 ``test_indexer_pins_catch_planted_mistakes`` plants mistakes in the oracle and
 checks that a pin fails for each.
@@ -136,6 +139,36 @@ def pin_dominance(seed=6) -> float:
     return 0.0
 
 
+def pin_zigzag_chunks_equal_full_document(seed=8) -> float:
+    """The pages' check of packed context-parallel chunks (Megatron-LM PR #14): the
+    zigzag chunks of one document (cp_size 2: rank r holds chunks r and 3 - r of 12
+    rows), each a segment over the key prefix that ends with it, bottom-right aligned
+    at q_causal_offset = its first global row, select exactly what the full-document
+    causal indexer selects for the same rows (overlap 1, nothing causally out of
+    bounds). The chunk-local top-left mask selects differently for the later chunks."""
+    rng = np.random.default_rng(seed)
+    n, c, H, d, topk = 48, 12, 2, 5, 6
+    q, k, w = rng.standard_normal((n, H, d)), rng.standard_normal((n, d)), rng.standard_normal((n, H))
+    full, _, _ = ix.indexer_topk(q, k, w, [0, n], [0, n], [0], [0], [0], [1], None, topk,
+                                 np.zeros((n, topk), dtype=np.int64))
+    chunks = [0, 3, 1, 2]                                       # rank 0, then rank 1
+    cu_q = np.concatenate([[0], np.cumsum([c] * 4)])
+    cu_k = np.concatenate([[0], np.cumsum([(ch + 1) * c for ch in chunks])])
+    starts = [ch * c for ch in chunks]
+    for masks, qco in (([2] * 4, starts), ([1] * 4, None)):
+        got, _, _ = ix.indexer_topk(q, k, w, cu_q, cu_k, starts, [0] * 4, starts, masks, qco, topk,
+                                    np.zeros((n, topk), dtype=np.int64))
+        if qco is not None:
+            assert (got == full).all(), "zigzag chunks disagree with the full document"
+            for ch in chunks:
+                rows = got[ch * c:(ch + 1) * c]
+                assert (rows < (np.arange(ch * c, (ch + 1) * c) + 1)[:, None]).all()
+        else:
+            assert (got[:c] == full[:c]).all()                  # chunk 0: local == global
+            assert not (got == full).all(), "a chunk-local mask should select differently"
+    return 0.0
+
+
 def pin_untouched_rows(seed=7) -> float:
     p = _pack(seed)
     idx, _, written = _run(p)
@@ -145,7 +178,7 @@ def pin_untouched_rows(seed=7) -> float:
 
 PINS = {"brute_force": pin_brute_force, "dot_product_special_case": pin_dot_product_special_case,
         "causal_bounds_and_counts": pin_causal_bounds_and_counts, "dominance": pin_dominance,
-        "untouched_rows": pin_untouched_rows}
+        "untouched_rows": pin_untouched_rows, "zigzag_chunks": pin_zigzag_chunks_equal_full_document}
 
 
 @pytest.mark.parametrize("name", sorted(PINS))
