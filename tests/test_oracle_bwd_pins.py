@@ -9,7 +9,10 @@
 * a special case with a closed form: a window of zero keys on a causal mask gives
   every live row exactly one key, so P = 1, dS = 0, dQ = dK = 0 and dV_j is the
   sum of dO over the rows that see key j;
-* untouched rows outside the sequences.
+* untouched rows outside the sequences;
+* the context-parallel crop: a bottom-right chunk at q_causal_offset c has the
+  gradients of full causal attention over its key prefix with dO = 0 on the
+  other query rows.
 
 ``test_bwd_pins_catch_planted_mistakes`` plants plausible mistakes in the oracle
 and checks that at least one pin fails for each.
@@ -148,6 +151,29 @@ def pin_single_key_window(seed=6) -> float:
     return worst
 
 
+def pin_cp_crop(seed=8) -> float:
+    """A context-parallel chunk (Megatron-LM PR #14): Lq query rows sitting at
+    absolute rows c .. c + Lq - 1 of an Lk-key prefix, bottom-right with
+    q_causal_offset = c, have the gradients of full causal self-attention over the
+    Lk rows whose other query rows carry dO = 0 (they add nothing: dP = D = 0 there).
+    dQ of the chunk = rows c .. c + Lq - 1 of the full dQ; dK and dV are equal."""
+    rng = np.random.default_rng(seed)
+    lk, c, lq, h, d = 11, 4, 5, 2, 3
+    q_full = rng.standard_normal((lk, h, d))
+    k, v = rng.standard_normal((lk, 1, d)), rng.standard_normal((lk, 1, d))
+    g_full = np.zeros((lk, h, d))
+    g_full[c:c + lq] = rng.standard_normal((lq, h, d))
+    z = np.zeros
+    full = tb.thd_attention_bwd(q_full, k, v, g_full, [0, lk], [0, lk], [0], [0], [0], [0], [1], None,
+                                z(q_full.shape), z(k.shape), z(v.shape))
+    chunk = tb.thd_attention_bwd(q_full[c:c + lq], k, v, g_full[c:c + lq], [0, lq], [0, lk], [0], [0], [0], [0],
+                                 [2], [c], z((lq, h, d)), z(k.shape), z(v.shape))
+    worst = max(float(np.abs(chunk[0] - full[0][c:c + lq]).max()), float(np.abs(chunk[1] - full[1]).max()),
+                float(np.abs(chunk[2] - full[2]).max()))
+    assert worst < 1e-12, f"CP chunk gradients differ from the full-prefix ones by {worst}"
+    return worst
+
+
 def pin_untouched_rows(seed=7) -> float:
     p = _tiny_pack(seed)
     dq, dk, dv, wq, wk, wv = _oracle(p)
@@ -165,6 +191,7 @@ PINS = {
     "invariants": pin_invariants,
     "single_key_window": pin_single_key_window,
     "untouched_rows": pin_untouched_rows,
+    "cp_crop": pin_cp_crop,
 }
 
 
