@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/thd_attn.h: descriptor validation,
 // capacity checks by the all-axes span rule (cudnn-frontend PR #462, "The fix"),
-// kernel selection, workspace layout, and the asynchronous fwd enqueue.
+// kernel selection, workspace layouts, and the asynchronous enqueue of the
+// forward, backward and indexer top-k passes.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>

@@ -1,4 +1,4 @@
-// Interface of the tcgen05 (tensor-core, TMEM, TMA) forward kernel.
+// Interface of the tcgen05 (tensor-core, TMEM, TMA) kernels: forward, backward and indexer scores.
 #pragma once
 
 #include "internal.h"
