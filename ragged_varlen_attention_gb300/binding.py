@@ -6,6 +6,7 @@ is no fallback -- when the library is missing the first call raises.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import math
 import os
@@ -390,7 +391,23 @@ def alloc_workspace(plan: ThdAttnPlan, device) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-_PLAN_CACHE: dict = {}
+# plans of the one-call wrappers, keyed by everything a plan depends on; bounded
+# (least recently used first out) so that a caller whose shapes keep changing does
+# not accumulate plans: an evicted plan is destroyed once nothing references it
+_PLAN_CACHE_SIZE = 64
+_PLAN_CACHE: "collections.OrderedDict[tuple, ThdAttnPlan]" = collections.OrderedDict()
+
+
+def _cached_plan(key: tuple, make):
+    plan = _PLAN_CACHE.get(key)
+    if plan is None:
+        plan = make()
+        _PLAN_CACHE[key] = plan
+        while len(_PLAN_CACHE) > _PLAN_CACHE_SIZE:
+            _PLAN_CACHE.popitem(last=False)
+    else:
+        _PLAN_CACHE.move_to_end(key)
+    return plan
 
 
 def thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=None, off_v=None,
@@ -421,10 +438,8 @@ def thd_attn_forward(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, off_q=None, off_k=
     key = (q.dtype, batch, tuple(q.shape), tuple(k.shape), tuple(v.shape), tuple(o.shape),
            q.stride(), k.stride(), v.stride(), o.stride(), cap_s, stats_layout, softmax_scale, kernel,
            _view_bytes(q), _view_bytes(k), _view_bytes(v), _view_bytes(o))
-    plan = _PLAN_CACHE.get(key)
-    if plan is None:
-        plan = plan_for_tensors(q, k, v, o, batch, cap_s, stats_layout, softmax_scale, kernel)
-        _PLAN_CACHE[key] = plan
+    plan = _cached_plan(key, lambda: plan_for_tensors(q, k, v, o, batch, cap_s, stats_layout, softmax_scale,
+                                                      kernel))
     if workspace is None:
         workspace = alloc_workspace(plan, dev)
     thd_attn_fwd_window(plan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
@@ -457,10 +472,8 @@ def thd_attn_backward(q, k, v, o, d_o, stats, cu_seqlens_q, cu_seqlens_kv, *, of
            q.stride(), k.stride(), v.stride(), o.stride(), d_o.stride(), dq.stride(), dk.stride(), dv.stride(),
            tuple(d_o.shape), tuple(dq.shape), tuple(dk.shape), tuple(dv.shape), cap_s, stats_layout,
            softmax_scale, kernel)
-    plan = _PLAN_CACHE.get(key)
-    if plan is None:
-        plan = plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch, cap_s, stats_layout, softmax_scale, kernel)
-        _PLAN_CACHE[key] = plan
+    plan = _cached_plan(key, lambda: plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch, cap_s, stats_layout,
+                                                          softmax_scale, kernel))
     if workspace is None:
         workspace = alloc_workspace(plan, dev)
     thd_attn_bwd(plan, q, k, v, o, d_o, stats, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
@@ -488,10 +501,8 @@ def thd_indexer(q_i, k_i, w, cu_seqlens_q, cu_seqlens_kv, topk: int, *, off_q=No
         score_out = torch.full((idx_out.shape[0], topk), float("nan"), dtype=torch.float32, device=dev)
     key = ("indexer", q_i.dtype, batch, tuple(q_i.shape), q_i.stride(), tuple(k_i.shape), k_i.stride(),
            w.stride(), tuple(idx_out.shape), topk, max_seqlen_k, kernel)
-    plan = _PLAN_CACHE.get(key)
-    if plan is None:
-        plan = indexer_plan_for_tensors(q_i, k_i, w, idx_out, batch, topk, max_seqlen_k, kernel)
-        _PLAN_CACHE[key] = plan
+    plan = _cached_plan(key, lambda: indexer_plan_for_tensors(q_i, k_i, w, idx_out, batch, topk, max_seqlen_k,
+                                                              kernel))
     if workspace is None:
         workspace = alloc_workspace(plan, dev)
     thd_indexer_topk(plan, q_i, k_i, w, idx_out, score_out, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_out,

@@ -262,3 +262,23 @@ def test_indexer_key_schedule_sized_per_segment(lib):
     assert all(st == 0 and k == bd.KERNEL_TCGEN05 for st, _, k in sizes)
     ws = [w for _, w, _ in sizes]
     assert ws[1] - ws[0] >= 3 * 16 * 16 and ws[2] - ws[1] >= 12 * 16 * 16
+
+
+def test_wrapper_plan_cache_is_bounded_lru(monkeypatch):
+    """The one-call wrappers' plan cache keeps the most recently used plans only, so
+    a caller whose shapes keep changing does not accumulate plans."""
+    import collections
+    monkeypatch.setattr(bd, "_PLAN_CACHE", collections.OrderedDict())
+    made = []
+
+    def make(i):
+        return lambda: made.append(i) or ("plan", i)
+
+    first = bd._cached_plan(("k", 0), make(0))
+    for i in range(1, bd._PLAN_CACHE_SIZE):
+        bd._cached_plan(("k", i), make(i))
+    assert bd._cached_plan(("k", 0), make(-1)) is first          # hit: moved to the newest end
+    bd._cached_plan(("k", "new"), make("new"))                    # evicts the oldest: key 1
+    assert len(bd._PLAN_CACHE) == bd._PLAN_CACHE_SIZE
+    assert ("k", 1) not in bd._PLAN_CACHE and ("k", 0) in bd._PLAN_CACHE
+    assert -1 not in made
