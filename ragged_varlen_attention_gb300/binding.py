@@ -214,6 +214,8 @@ def plan_for_tensors(q, k, v, o, batch: int, cap_rows_stats: int, stats_layout: 
     for t in (q, k, v, o):
         if t.dim() != 3 or t.stride(2) != 1:
             raise ValueError("Q/K/V/O must be [rows, heads, d] views with a contiguous last dim")
+        if t.dtype != q.dtype:
+            raise ValueError("Q, K, V and O must share one storage type")
     desc = make_desc(q.dtype, batch, q.shape[1], k.shape[1], q.shape[2],
                      [t.shape[0] for t in (q, k, v, o)], [t.stride(0) for t in (q, k, v, o)],
                      [t.stride(1) for t in (q, k, v, o)], [_view_bytes(t) for t in (q, k, v, o)],
@@ -229,6 +231,8 @@ def plan_bwd_for_tensors(q, k, v, o, d_o, dq, dk, dv, batch: int, cap_rows_stats
     for t in (q, k, v, o, d_o, dq, dk, dv):
         if t.dim() != 3 or t.stride(2) != 1:
             raise ValueError("tensors must be [rows, heads, d] views with a contiguous last dim")
+        if t.dtype != q.dtype:
+            raise ValueError("the forward's tensors and the gradients must share one storage type")
     bd = ThdAttnBwdDesc()
     bd.fwd = make_desc(q.dtype, batch, q.shape[1], k.shape[1], q.shape[2],
                        [t.shape[0] for t in (q, k, v, o)], [t.stride(0) for t in (q, k, v, o)],
@@ -254,6 +258,8 @@ def indexer_plan_for_tensors(q_i, k_i, w, idx_out, batch: int, topk: int, max_se
     stride 1) and the int32 [rows, topk] output (see ``thd_indexer_plan``)."""
     if q_i.dim() != 3 or q_i.stride(2) != 1 or k_i.dim() != 2 or k_i.stride(1) != 1:
         raise ValueError("QI must be [rows, H, d] and KI [rows, d] with a contiguous last dim")
+    if k_i.dtype != q_i.dtype:
+        raise ValueError("QI and KI must share one storage type")
     if w.dtype != torch.float32 or w.dim() != 2 or w.stride(1) != 1:
         raise ValueError("W must be float32 [rows, H] with head stride 1")
     if idx_out.dtype != torch.int32 or idx_out.dim() != 2 or idx_out.shape[1] != topk or not idx_out.is_contiguous():

@@ -282,3 +282,19 @@ def test_wrapper_plan_cache_is_bounded_lru(monkeypatch):
     assert len(bd._PLAN_CACHE) == bd._PLAN_CACHE_SIZE
     assert ("k", 1) not in bd._PLAN_CACHE and ("k", 0) in bd._PLAN_CACHE
     assert -1 not in made
+
+
+def test_plan_builders_reject_mixed_storage_types(lib):
+    """One descriptor dtype covers every tensor of a plan: mixed storage types are
+    a caller error, refused before any plan exists."""
+    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(8, 2, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        bd.plan_for_tensors(q, k, q, q, 1, 8, bd.STATS_TOKEN_MAJOR)
+    with pytest.raises(ValueError):
+        bd.plan_bwd_for_tensors(q, q, q, q, q, q, k, q, 1, 8, bd.STATS_TOKEN_MAJOR)
+    w = torch.zeros(8, 2, dtype=torch.float32)
+    idx = torch.zeros(8, 4, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        bd.indexer_plan_for_tensors(q, torch.zeros(8, 64, dtype=torch.float16), w, idx, 1, 4)
+    assert bd.plan_for_tensors(q, q, q, q, 1, 8, bd.STATS_TOKEN_MAJOR).workspace_bytes > 0
