@@ -185,6 +185,21 @@ def max_over_ranks(dist, x: float, device) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(dist, x: float, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Seed of rank ``rank``'s batch: in a multi-GPU run every rank draws its own
+    batch of the workload's shape (its shard of the job; the units are independent,
+    so no data crosses ranks); rank 0 keeps the workload's own seed."""
+    return base + 1000 * rank
+
+
 def oracle_sample_time(batch, budget_s: float, max_rows: int | None = None):
     """Run the oracle on row slices of the workload until ``budget_s`` elapses.
 
@@ -283,7 +298,8 @@ def config_block(args, batch):
             "window_left": None if batch.window_left is None else int(batch.window_left[0]),
             "l2": "inputs larger than L2 (K/V alone exceed 129 MB); no flush between steps"
             if valid_bytes(batch) > 129e6 else "inputs smaller than L2; L2 flushed between timed steps",
-            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+            "parallelism": (f"data-parallel x{args.gpus}, a batch per rank" if args.gpus > 1
+                            else "single GPU")}
 
 
 def main():
@@ -315,7 +331,8 @@ def main():
         else:
             bench_indexer(args)
         return
-    batch = wl.make(args.workload)
+    env_rank = int(os.environ.get("RANK", "0"))
+    batch = wl.make(args.workload, seed=rank_seed(wl.WORKLOAD_SEEDS[args.workload], env_rank))
     if args.window_left is not None:
         import dataclasses
         batch = dataclasses.replace(batch, window_left=np.full(batch.batch, args.window_left, dtype=np.int32))
@@ -408,7 +425,8 @@ def main():
     kernel_ms, kernel_launches = bd.profile_read(plan)
     bd.profile_enable(plan, 0)
     ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
-    value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+    flop_all = sum_over_ranks(dist, flop_per_step, device)      # every rank's own batch
+    value = flop_all / (ms_per_step * 1e-3) / 1e12
 
     # the same step replayed from a CUDA graph (the call is capturable: no host
     # synchronisation, no allocation)
@@ -475,7 +493,7 @@ def main():
     ev1.record(stream)
     barrier(dist, device)
     e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / args.e2e_steps, device)
-    e2e_value = flop_per_step * world / (e2e_ms * 1e-3) / 1e12
+    e2e_value = flop_all / (e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
@@ -644,7 +662,8 @@ def bench_backward(args, batch, bd, kernel, device, dist, rank, world):
     kernel_ms, kernel_launches = bd.profile_read(plan)
     bd.profile_enable(plan, 0)
     ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
-    value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+    flop_all = sum_over_ranks(dist, flop_per_step, device)      # every rank's own batch
+    value = flop_all / (ms_per_step * 1e-3) / 1e12
 
     h2d_t = [host[n] for n in ("q", "k", "v", "d_o", "cu_q", "cu_k", "mask")] + host["offs"] + [o_host, stats_host]
     h2d_t += [host[n] for n in ("qco", "win") if host[n] is not None]
@@ -689,7 +708,7 @@ def bench_backward(args, batch, bd, kernel, device, dist, rank, world):
                      if peak_src == "measured" else "fallback 1.9 PFLOP/s",
                      "kernel": "dQ kernel + dK/dV kernel (CUDA events on their stream around both)",
                      "kernel_ms": kernel_ms, "launches": kernel_launches, "traffic": None},
-        "e2e": {"value": flop_per_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": flop_all / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                 "steps": args.e2e_steps},
         "gpu_launches": 5 * args.steps,
@@ -758,7 +777,7 @@ def bench_indexer(args):
     if dist is not None:
         dist.barrier()
     kernel = {"auto": bd.KERNEL_AUTO, "simt": bd.KERNEL_SIMT, "tcgen05": bd.KERNEL_TCGEN05}[args.kernel]
-    b = wl.indexer_cp()
+    b = wl.indexer_cp(seed=rank_seed(wl.INDEXER_CP_SEED, rank))
     ints = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt))
     host = {"q": b.q.pin_memory(), "k": b.k.pin_memory(), "w": b.w.pin_memory(),
             "cu_q": ints(b.cu_seqlens_q).pin_memory(), "cu_k": ints(b.cu_seqlens_kv).pin_memory(),
@@ -801,7 +820,8 @@ def bench_indexer(args):
     kernel_ms, launches = bd.profile_read(plan)
     bd.profile_enable(plan, 0)
     ms_per_step = max_over_ranks(dist, total_ms / args.steps, device)
-    value = flop_per_step * world / (ms_per_step * 1e-3) / 1e12
+    flop_all = sum_over_ranks(dist, flop_per_step, device)      # every rank's own batch
+    value = flop_all / (ms_per_step * 1e-3) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = idx_host.numel() * 4 + sc_host.numel() * 4
 
@@ -832,7 +852,8 @@ def bench_indexer(args):
                    "visible_pairs": pairs, "flop_per_step": flop_per_step, "pass": "indexer",
                    "kernel": "tcgen05" if tc else "simt",
                    "l2": "inputs smaller than L2 but the float32 score scratch (2 GB) is not; no flush",
-                   "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"},
+                   "parallelism": (f"data-parallel x{args.gpus}, a batch per rank" if args.gpus > 1
+                                   else "single GPU")},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": kt, "peak": peak, "unit": "TFLOP/s",
                      "frac": None if kt is None else kt / peak,
@@ -840,7 +861,7 @@ def bench_indexer(args):
                      if peak_src == "measured" else "fallback 1.9 PFLOP/s",
                      "kernel": "indexer score kernel (CUDA events on its stream)",
                      "kernel_ms": kernel_ms, "launches": launches, "traffic": None},
-        "e2e": {"value": flop_per_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": flop_all / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                 "steps": args.e2e_steps},
         "gpu_launches": (4 if tc else 3) * args.steps,

@@ -311,7 +311,10 @@ class IndexerBatch:
         return np.diff(self.cu_seqlens_kv)
 
 
-def indexer_cp(seed: int = 106, docs: int = 2, k_len: int = 65536, q_len: int = 4096, heads: int = 64,
+INDEXER_CP_SEED = 106
+
+
+def indexer_cp(seed: int = INDEXER_CP_SEED, docs: int = 2, k_len: int = 65536, q_len: int = 4096, heads: int = 64,
                d: int = 128, topk: int = 2048, dtype: str = "bf16") -> IndexerBatch:
     """Context-parallel indexer chunks (the Megatron-LM PR #14 multi-document case):
     per document a packed key prefix of ``k_len`` tokens and a ``q_len``-row query
