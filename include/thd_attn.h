@@ -237,16 +237,18 @@ int64_t thd_attn_view_span_bytes(int64_t rows, int64_t heads, int64_t d, int64_t
  * Same arguments and results as thd_attn_fwd minus `workspace`. The scratch is a
  * static device array of thd_attn_static_workspace_capacity() bytes (1 MiB) that
  * each GPU loading this library keeps until the process exits. The call makes no
- * allocation of any kind. Returns THD_ERR_WORKSPACE when the plan's
- * workspace_bytes exceed that capacity (plan with THD_FLAG_NO_KV_SPLIT: the
- * partial results of split key ranges do not fit the static array).
+ * allocation of any kind. Returns THD_ERR_INVALID_ARG for a backward or indexer
+ * plan, and THD_ERR_WORKSPACE when a forward plan's workspace_bytes exceed that
+ * capacity (plan with THD_FLAG_NO_KV_SPLIT: the partial results of split key
+ * ranges do not fit the static array).
  *
  * The first call on each device (with that device current) looks up the array's
  * device address with cudaGetSymbolAddress; make it before any stream capture.
  * All calls on a device share the array, which keeps the previous call's
  * contents (each call rewrites what it reads before reading it). Calls that
  * overlap on the GPU -- e.g. on unordered streams -- race on the array. The
- * device status word of these calls lives in that array and is not exposed. */
+ * device status word of these calls lives in that array: read it with
+ * thd_attn_static_read_status. */
 thd_status_t thd_attn_fwd_static_ws(thd_attn_plan_t plan, const void* q, const void* k, const void* v,
                                     void* o, float* stats, const int32_t* cu_seqlens_q,
                                     const int32_t* cu_seqlens_kv, const int32_t* off_q,
@@ -256,6 +258,14 @@ thd_status_t thd_attn_fwd_static_ws(thd_attn_plan_t plan, const void* q, const v
 
 /* Capacity in bytes of the static scratch array used by thd_attn_fwd_static_ws. */
 size_t thd_attn_static_workspace_capacity(void);
+
+/* thd_attn_read_status for calls made through thd_attn_fwd_static_ws: copies the
+ * device status word that the last such call on the current device left in the
+ * static array (THD_DEV_* bits) to *host_out and synchronises `stream`. `plan`
+ * must be the forward plan of that call. Like thd_attn_fwd_static_ws it has no
+ * counterpart in the pages; it waits on the device, so it is not for use while a
+ * stream is being captured. */
+thd_status_t thd_attn_static_read_status(thd_attn_plan_t plan, uint32_t* host_out, void* stream);
 
 /* ------------------------------------------------------------------ backward
  *

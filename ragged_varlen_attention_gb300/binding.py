@@ -88,6 +88,7 @@ _EXPORTS = ["thd_attn_plan", "thd_attn_fwd", "thd_attn_read_status", "thd_attn_p
             "thd_attn_plan_geometry", "thd_attn_plan_workspace_layout", "thd_attn_plan_destroy",
             "thd_attn_status_string", "thd_attn_view_span_bytes", "thd_attn_profile_enable",
             "thd_attn_profile_read", "thd_attn_fwd_static_ws", "thd_attn_static_workspace_capacity",
+            "thd_attn_static_read_status",
             "thd_attn_fwd_window", "thd_attn_plan_bwd", "thd_attn_bwd", "thd_indexer_plan",
             "thd_indexer_topk"]
 
@@ -145,6 +146,8 @@ def load_library():
     lib.thd_attn_fwd_static_ws.restype = ctypes.c_int
     lib.thd_attn_static_workspace_capacity.argtypes = []
     lib.thd_attn_static_workspace_capacity.restype = ctypes.c_size_t
+    lib.thd_attn_static_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.thd_attn_static_read_status.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -363,6 +366,17 @@ def thd_attn_fwd_static_ws(plan: ThdAttnPlan, q, k, v, o, stats, cu_seqlens_q, c
 
 def static_workspace_capacity() -> int:
     return int(load_library().thd_attn_static_workspace_capacity())
+
+
+def thd_attn_static_read_status(plan: ThdAttnPlan, stream=None) -> int:
+    """Device status word (THD_DEV_* bits) of the last ``thd_attn_fwd_static_ws`` call
+    on the current device; synchronises ``stream``."""
+    out = ctypes.c_uint32()
+    st = load_library().thd_attn_static_read_status(ctypes.c_void_p(plan.handle), ctypes.byref(out),
+                                                     _stream_handle(stream))
+    if st != 0:
+        raise ThdAttnError(st, "thd_attn_static_read_status")
+    return out.value
 
 
 def thd_attn_read_status(plan: ThdAttnPlan, workspace, stream=None) -> int:

@@ -22,6 +22,7 @@
 // zeroes) before the attention kernel starts, so no clearing is needed between
 // calls. Calls whose kernels overlap on the GPU (for example, on two streams
 // without ordering between them) race on the array and must not be made.
+#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -33,7 +34,23 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-void* g_device_address[kMaxDevices] = {nullptr};
+// Device address of the array per device. Two host threads making their first
+// call on a device at once may both resolve it; they store the same value.
+std::atomic<void*> g_device_address[kMaxDevices];
+
+// The array's device address on the current device (resolved once per device).
+thd_status_t static_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return THD_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return THD_ERR_CUDA;
+  void* ptr = g_device_address[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return THD_ERR_CUDA;
+    g_device_address[dev].store(ptr, std::memory_order_release);
+  }
+  *out = ptr;
+  return THD_OK;
+}
 
 }  // namespace
 
@@ -46,18 +63,22 @@ thd_status_t thd_attn_fwd_static_ws(thd_attn_plan_t plan, const void* q, const v
                                     const int32_t* cu_seqlens_kv, const int32_t* off_q, const int32_t* off_k,
                                     const int32_t* off_v, const int32_t* off_o, const int32_t* off_s,
                                     const int8_t* mask_type, const int32_t* q_causal_offset, void* stream) {
-  if (!plan) return THD_ERR_INVALID_ARG;
+  // only forward plans run here, whatever their workspace size
+  if (!plan || plan->is_bwd || plan->is_indexer) return THD_ERR_INVALID_ARG;
   if (plan->ws_bytes > kStaticWorkspaceBytes) return THD_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return THD_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return THD_ERR_CUDA;
-  if (!g_device_address[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return THD_ERR_CUDA;
-    g_device_address[dev] = ptr;
-  }
+  void* ws = nullptr;
+  const thd_status_t st = static_address(&ws);
+  if (st != THD_OK) return st;
   return thd_attn_fwd(plan, q, k, v, o, stats, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v, off_o, off_s,
-                      mask_type, q_causal_offset, g_device_address[dev], stream);
+                      mask_type, q_causal_offset, ws, stream);
+}
+
+thd_status_t thd_attn_static_read_status(thd_attn_plan_t plan, uint32_t* host_out, void* stream) {
+  if (!plan || !host_out || plan->is_bwd || plan->is_indexer) return THD_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const thd_status_t st = static_address(&ws);
+  if (st != THD_OK) return st;
+  return thd_attn_read_status(plan, ws, host_out, stream);
 }
 
 }  // extern "C"

@@ -213,6 +213,36 @@ def test_fwd_rejects_backward_and_indexer_plans(lib):
     lib.thd_attn_plan_destroy(h)
 
 
+def test_static_entry_rejects_non_forward_plans_before_capacity(lib):
+    """The workspace-free entry point refuses backward and indexer plans with
+    THD_ERR_INVALID_ARG whatever their workspace size, and a forward plan larger than
+    its static array with THD_ERR_WORKSPACE; all before any CUDA call."""
+    cap = lib.thd_attn_static_workspace_capacity()
+    out = ctypes.c_uint32()
+    small_bwd = _bwd_desc()
+    big_bwd = _bwd_desc()
+    big_bwd.fwd.batch = cap // 32 + 1
+    ix = _ix_desc()
+    for make, desc in ((lib.thd_attn_plan_bwd, small_bwd), (lib.thd_attn_plan_bwd, big_bwd),
+                       (lib.thd_indexer_plan, ix)):
+        h = ctypes.c_void_p()
+        ws = ctypes.c_size_t()
+        assert make(ctypes.byref(h), ctypes.byref(desc), ctypes.byref(ws)) == 0
+        args = [h] + [ctypes.c_void_p(256)] * 14 + [ctypes.c_void_p(0)]
+        assert lib.thd_attn_fwd_static_ws(*args) == 1
+        assert lib.thd_attn_static_read_status(h, ctypes.byref(out), ctypes.c_void_p(0)) == 1
+        lib.thd_attn_plan_destroy(h)
+    big = bd.make_desc(torch.bfloat16, cap // 32 + 1, 1, 1, 64, (1, 1, 1, 1), (64, 64, 64, 64),
+                       (64, 64, 64, 64), cap_rows_stats=1)
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    assert lib.thd_attn_plan(ctypes.byref(h), ctypes.byref(big), ctypes.byref(ws)) == 0
+    assert ws.value > cap
+    args = [h] + [ctypes.c_void_p(256)] * 14 + [ctypes.c_void_p(0)]
+    assert lib.thd_attn_fwd_static_ws(*args) == 5
+    lib.thd_attn_plan_destroy(h)
+
+
 # ------------------------------------------------------------------- indexer plans
 def _ix_desc(**kw):
     d = bd.ThdIndexerDesc()
