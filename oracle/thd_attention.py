@@ -77,13 +77,6 @@ def window_lower_shift(mask_type: int, shift: int | None, window_left) -> int | 
     return shift - int(window_left)
 
 
-def visible_key_count(i: int, len_k: int, shift: int | None, lower: int | None = None) -> int:
-    """Number of keys visible to query row ``i``."""
-    hi = len_k if shift is None else max(0, min(len_k, i + shift + 1))
-    lo = 0 if lower is None else max(0, i + lower)
-    return max(0, hi - lo)
-
-
 def attention_one_head(qb: np.ndarray, kb: np.ndarray, vb: np.ndarray, scale: float,
                        shift: int | None, rows: slice | None = None, lower: int | None = None):
     """O and LSE of one sequence and one query head, float64.
@@ -176,9 +169,13 @@ def thd_attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, off_v,
                 idx = np.array(rows, dtype=np.int64)
                 ob = np.zeros((len(idx), v.shape[2]))
                 lb = np.full((len(idx),), -np.inf)
-                for n, r in enumerate(idx):
-                    ob[n:n + 1], lb[n:n + 1] = attention_one_head(qb, kb, vb, scale, shift,
-                                                                  rows=slice(r, r + 1), lower=lower)
+                # runs of consecutive rows are evaluated together (rows are independent)
+                starts = np.flatnonzero(np.diff(idx, prepend=-2) != 1)
+                ends = np.append(starts[1:], len(idx))
+                for a, e in zip(starts, ends):
+                    ob[a:e], lb[a:e] = attention_one_head(qb, kb, vb, scale, shift,
+                                                          rows=slice(int(idx[a]), int(idx[e - 1]) + 1),
+                                                          lower=lower)
             o[os_ + idx, h, :] = ob
             stats[(ss + idx) * stats_stride_tok + h * stats_stride_head] = lb
         if rows is None:

@@ -550,3 +550,31 @@ def test_pins_catch_planted_mistakes(monkeypatch, target, mutant):
         if not err <= tol:
             failed.append(name)
     assert failed, f"no pin caught the planted mistake {mutant.__name__}"
+
+
+def test_row_subset_matches_brute_force_rows():
+    """A row subset (single rows and runs of consecutive rows, in any order) gives
+    the scalar brute force's values on exactly those rows and writes no other row."""
+    batch = wl.random_pack(23, batch=3, max_len=40, h_q=2, h_kv=1, d=8, dtype="fp32", with_qco=True)
+    lq = batch.lens_q()
+    subset = {b: sorted({0, int(lq[b]) - 1, *range(3, 9), 11, 12, 20}) for b in range(batch.batch)}
+    o_sub, s_sub, w_sub = oracle_on_batch(batch, row_subset=subset)
+    st_tok, st_head = batch.stats_strides
+    o_b, s_b = brute_attention(as_f64(batch.q).tolist(), as_f64(batch.k).tolist(), as_f64(batch.v).tolist(),
+                               list(batch.cu_seqlens_q), list(batch.cu_seqlens_kv), list(batch.off_q),
+                               list(batch.off_k), list(batch.off_v), list(batch.off_o), list(batch.off_s),
+                               list(batch.mask_type), None if batch.q_causal_offset is None
+                               else list(batch.q_causal_offset), as_f64(batch.o_init()).tolist(),
+                               batch.stats_init().to(torch.float64).tolist(), st_tok, st_head)
+    o_b, s_b = np.array(o_b), np.array(s_b)
+    want = np.zeros(batch.cap_o, dtype=bool)
+    for b in range(batch.batch):
+        rows = [r for r in subset[b] if 0 <= r < lq[b]]
+        want[batch.off_o[b] + np.array(rows, dtype=np.int64)] = True
+        for h in range(batch.h_q):
+            idx = (batch.off_s[b] + np.array(rows, dtype=np.int64)) * st_tok + h * st_head
+            assert max_abs_finite(s_sub[idx], s_b[idx]) < 1e-12
+    assert np.array_equal(w_sub, want)
+    assert float(np.max(np.abs(o_sub[want] - o_b[want]), initial=0.0)) < 1e-12
+    init = as_f64(batch.o_init())
+    assert np.array_equal(o_sub[~want].view(np.uint64), init[~want].view(np.uint64))
