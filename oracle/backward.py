@@ -26,6 +26,11 @@ one sequence and one query head at a time, float64:
 * Gradient tensors share their primal tensor's row offsets (``dQ`` at
   ``off_q``, ``dK`` at ``off_k``, ``dV`` at ``off_v``; ``dO`` is read at
   ``off_o``). Rows outside ``[off[b], off[b] + len[b])`` keep their prior values.
+* Segments may share key rows: the zigzag query chunks of one document under
+  context parallelism all attend to its key prefix (Megatron-LM PR #14, the
+  packed-CP paths). The loss sums over every segment, so a K or V row read by
+  several segments gets the SUM of their contributions (chain rule); a written
+  row's prior content is replaced, never added to.
 
 The saved forward Stats and O are not inputs here: the oracle recomputes P
 from Q and K, so a kernel that reads Stats or O at the wrong place disagrees.
@@ -103,6 +108,9 @@ def thd_attention_bwd(q, k, v, d_o, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, o
     wq = np.zeros((dq.shape[0],), dtype=bool)
     wk = np.zeros((dk.shape[0],), dtype=bool)
     wv = np.zeros((dv.shape[0],), dtype=bool)
+    # key and value gradients summed over every segment that reads a row
+    sum_k = np.zeros_like(dk)
+    sum_v = np.zeros_like(dv)
     for b in range(len(cu_seqlens_q) - 1):
         len_q = int(cu_seqlens_q[b + 1]) - int(cu_seqlens_q[b])
         len_k = int(cu_seqlens_kv[b + 1]) - int(cu_seqlens_kv[b])
@@ -121,9 +129,11 @@ def thd_attention_bwd(q, k, v, d_o, cu_seqlens_q, cu_seqlens_kv, off_q, off_k, o
             dq[qs:qs + len_q, h] = gq
             acc_k[:, g] += gk
             acc_v[:, g] += gv
-        dk[ks:ks + len_k] = acc_k
-        dv[vs:vs + len_k] = acc_v
+        sum_k[ks:ks + len_k] += acc_k
+        sum_v[vs:vs + len_k] += acc_v
         wq[qs:qs + len_q] = True
         wk[ks:ks + len_k] = True
         wv[vs:vs + len_k] = True
+    dk[wk] = sum_k[wk]
+    dv[wv] = sum_v[wv]
     return dq, dk, dv, wq, wk, wv

@@ -12,7 +12,11 @@
 * untouched rows outside the sequences;
 * the context-parallel crop: a bottom-right chunk at q_causal_offset c has the
   gradients of full causal attention over its key prefix with dO = 0 on the
-  other query rows.
+  other query rows;
+* segments that share key rows (the zigzag chunks of one document, Megatron-LM
+  PR #14): finite differences on a pack whose segments read the same K/V rows,
+  and the zigzag chunks' summed dK / dV equal those of full causal attention
+  over the document with dO = 0 outside the chunks.
 
 ``test_bwd_pins_catch_planted_mistakes`` plants plausible mistakes in the oracle
 and checks that at least one pin fails for each.
@@ -73,11 +77,11 @@ def _brute_loss(p, q, k, v, scale):
     return tot
 
 
-def pin_finite_differences(seeds=(1, 2)) -> float:
+def pin_finite_differences(seeds=(1, 2), make=_tiny_pack) -> float:
     """Max relative error of the oracle's gradients against central differences."""
     worst = 0.0
     for seed in seeds:
-        p = _tiny_pack(seed)
+        p = make(seed)
         scale = 0.7
         dq, dk, dv, wq, wk, wv = _oracle(p, scale)
         eps = 1e-6
@@ -174,6 +178,59 @@ def pin_cp_crop(seed=8) -> float:
     return worst
 
 
+def _shared_key_pack(seed):
+    """Three segments over one set of key rows (prefixes of it, each bottom-right
+    at its own offset), a fourth with keys of its own, gaps between query rows."""
+    rng = np.random.default_rng(seed)
+    h_q, h_kv, d = 2, 1, 3
+    lq = np.array([3, 2, 2, 3])
+    lk = np.array([6, 4, 6, 4])
+    off_q = np.array([1, 6, 10, 14])
+    off_k = np.array([0, 0, 0, 8])
+    cap_q, cap_k = 19, 13
+    return dict(q=rng.standard_normal((cap_q, h_q, d)), k=rng.standard_normal((cap_k, h_kv, d)),
+                v=rng.standard_normal((cap_k, h_kv, d)), g=rng.standard_normal((cap_q, h_q, d)),
+                cu_q=np.concatenate([[0], np.cumsum(lq)]), cu_k=np.concatenate([[0], np.cumsum(lk)]),
+                off_q=off_q, off_k=off_k, masks=np.array([2, 2, 0, 1]), qco=np.array([3, 2, 0, 0]),
+                window=np.array([-1, 1, -1, -1]))
+
+
+def pin_shared_keys_finite_differences(seed=9) -> float:
+    """Central differences of the brute-force loss on a pack whose segments share
+    K/V rows: a shared row's gradient is the sum over the segments reading it."""
+    return pin_finite_differences(seeds=(seed,), make=_shared_key_pack)
+
+
+def pin_zigzag_chunks(seed=10) -> float:
+    """The zigzag query chunks of one document (chunks r and 2*cp-1-r of 2*cp equal
+    chunks, cp = 2) as four segments over the SAME key rows, each bottom-right at its
+    chunk start over the key prefix that ends with it: dQ of each chunk equals the
+    full-document causal dQ of those rows, and the summed dK / dV equal the full
+    ones when dO is zero on rows outside the chunks (here: none are outside)."""
+    rng = np.random.default_rng(seed)
+    doc, n_chunks, h, d = 16, 4, 2, 3
+    c = doc // n_chunks
+    q_full = rng.standard_normal((doc, h, d))
+    k, v = rng.standard_normal((doc, 1, d)), rng.standard_normal((doc, 1, d))
+    g_full = rng.standard_normal((doc, h, d))
+    z = np.zeros
+    full = tb.thd_attention_bwd(q_full, k, v, g_full, [0, doc], [0, doc], [0], [0], [0], [0], [1], None,
+                                z(q_full.shape), z(k.shape), z(v.shape))
+    order = [0, 3, 1, 2]                              # rank 0: chunks 0, 3; rank 1: chunks 1, 2
+    q_seg = np.concatenate([q_full[x * c:(x + 1) * c] for x in order])
+    g_seg = np.concatenate([g_full[x * c:(x + 1) * c] for x in order])
+    cu_q = np.arange(0, len(order) * c + 1, c)
+    lk = [(x + 1) * c for x in order]
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    seg = tb.thd_attention_bwd(q_seg, k, v, g_seg, cu_q, cu_k, cu_q[:-1], [0] * 4, [0] * 4, cu_q[:-1],
+                               [2] * 4, [x * c for x in order], z(q_seg.shape), z(k.shape), z(v.shape))
+    dq_want = np.concatenate([full[0][x * c:(x + 1) * c] for x in order])
+    worst = max(float(np.abs(seg[0] - dq_want).max()), float(np.abs(seg[1] - full[1]).max()),
+                float(np.abs(seg[2] - full[2]).max()))
+    assert worst < 1e-12, f"zigzag chunk gradients differ from the full-document ones by {worst}"
+    return worst
+
+
 def pin_untouched_rows(seed=7) -> float:
     p = _tiny_pack(seed)
     dq, dk, dv, wq, wk, wv = _oracle(p)
@@ -192,6 +249,8 @@ PINS = {
     "single_key_window": pin_single_key_window,
     "untouched_rows": pin_untouched_rows,
     "cp_crop": pin_cp_crop,
+    "shared_keys_finite_differences": pin_shared_keys_finite_differences,
+    "zigzag_chunks": pin_zigzag_chunks,
 }
 
 
@@ -246,6 +305,32 @@ def test_bwd_pins_catch_planted_mistakes(monkeypatch, mistake):
         except AssertionError:
             failed.append(name)
     assert failed, f"no pin caught the planted mistake {mistake}"
+
+
+def test_shared_key_overwrite_mistake_is_caught(monkeypatch):
+    """Writing each segment's dK / dV over the rows (the last segment wins) instead
+    of summing the segments that share them."""
+    orig = tb.thd_attention_bwd
+
+    def overwrite(q, k, v, d_o, cu_q, cu_k, off_q, off_k, off_v, off_o, masks, qco, dq0, dk0, dv0, **kw):
+        dq, dk, dv = np.array(dq0, dtype=float), np.array(dk0, dtype=float), np.array(dv0, dtype=float)
+        wq, wk, wv = (np.zeros(len(x), dtype=bool) for x in (dq, dk, dv))
+        win = kw.pop("window_left", None)
+        for b in range(len(cu_q) - 1):
+            lq, lk = int(cu_q[b + 1] - cu_q[b]), int(cu_k[b + 1] - cu_k[b])
+            one = orig(q, k, v, d_o, [0, lq], [0, lk], [off_q[b]], [off_k[b]], [off_v[b]], [off_o[b]], [masks[b]],
+                       None if qco is None else [qco[b]], dq, dk, dv,
+                       window_left=None if win is None else [win[b]], **kw)
+            dq, dk, dv = one[0], one[1], one[2]
+            wq |= one[3]
+            wk |= one[4]
+            wv |= one[5]
+        return dq, dk, dv, wq, wk, wv
+
+    monkeypatch.setattr(tb, "thd_attention_bwd", overwrite)
+    for pin in (pin_shared_keys_finite_differences, pin_zigzag_chunks):
+        with pytest.raises(AssertionError):
+            pin()
 
 
 def test_gqa_head_map_mistake_is_caught(monkeypatch):
