@@ -91,7 +91,10 @@ enum {
   THD_DEV_BAD_OFFSET = 1u << 1,     /* off[b] < 0 or off[b] + len > cap_rows for some tensor */
   THD_DEV_BAD_MASK = 1u << 2,       /* mask_type[b] not in {0, 1, 2} */
   THD_DEV_TILE_OVERFLOW = 1u << 3,  /* more work units than the plan's capacity (no work done) */
-  THD_DEV_WAIT_TIMEOUT = 1u << 4    /* a bounded in-kernel wait gave up (kernel returned early) */
+  THD_DEV_WAIT_TIMEOUT = 1u << 4,   /* a bounded in-kernel wait gave up (kernel returned early) */
+  THD_DEV_KEY_OVERLAP = 1u << 5     /* backward: K or V rows of two sequences overlap without the
+                                       sequences forming one key group (see thd_attn_bwd); no dK
+                                       or dV row is written */
 };
 
 /* Host-known problem description, fixed per plan. Index 0..3 of the stride and
@@ -310,8 +313,16 @@ thd_status_t thd_attn_plan_bwd(thd_attn_plan_t* out, const thd_attn_bwd_desc_t* 
  *   dq, dk, dv         gradient views of the plan (written rows only)
  *   remaining metadata as in thd_attn_fwd_window (window_left may be NULL)
  * Asynchronous, no allocation, no device->host read; device data errors surface
- * through thd_attn_read_status. Gradient rows of different sequences that overlap
- * race. */
+ * through thd_attn_read_status.
+ *
+ * Sequences may share key rows: consecutive sequences whose off_k AND off_v are
+ * equal form one key group (e.g. the zigzag query chunks of one document under
+ * context parallelism, each bottom-right at its own q_causal_offset over a prefix
+ * of the document's keys; Megatron-LM PR #14). Each dK / dV row of a group is the
+ * sum over all of its members that see the key, and is written once. K or V rows
+ * shared in any other way (partial overlaps, equal offsets that are not adjacent
+ * in the batch) set THD_DEV_KEY_OVERLAP and no dK / dV row is written. dQ rows of
+ * different sequences that overlap race. */
 thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, const void* v,
                           const void* o, const void* d_o, const float* stats, void* dq, void* dk,
                           void* dv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,

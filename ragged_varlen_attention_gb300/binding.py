@@ -25,6 +25,7 @@ _STATUS = {0: "THD_OK", 1: "THD_ERR_INVALID_ARG", 2: "THD_ERR_UNSUPPORTED",
 
 # device status word bits
 DEV_BAD_LENGTH, DEV_BAD_OFFSET, DEV_BAD_MASK, DEV_TILE_OVERFLOW, DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+DEV_KEY_OVERLAP = 32
 
 
 class ThdAttnError(RuntimeError):

@@ -542,6 +542,7 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   bp.pairs_q = sp.pairs;
   // key axis: dK/dV units of kBwdKeysPerUnit keys, cost in query tiles
   sp.key_axis = 1;
+  sp.group_keys = 1;
   sp.unit_heads = d.h_kv;
   sp.rows_per_unit = thd::kBwdKeysPerUnit;
   sp.keys_per_tile = plan->rows_per_unit;

@@ -199,11 +199,15 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(BwdParams p) {
     int pair_idx, g;
     work_to_unit(p.header_k, w, p.h_kv, p.h_kv, pair_idx, g);
     const PairRec pr = p.pairs_k[pair_idx];
-    const SeqMeta m = p.meta[pr.b];
+    // the unit's key group: sequences pr.b .. pr.b + group_n - 1 read the same K/V
+    // rows (keys < group_len_k); each adds the gradient of its own query rows
+    const SeqMeta lead = p.meta[pr.b];
+    const int n_mem = max(1, lead.group_n);
     for (int sub = 0; sub < p.keys_per_unit; sub += KEYS) {
-      if (pr.row0 + sub >= m.len_k) break;   // uniform across the block
-      const int j = pr.row0 + sub + lkey;    // key inside the sequence
-      const bool live = j < m.len_k;
+      if (pr.row0 + sub >= lead.group_len_k) break;   // uniform across the block
+      const int j = pr.row0 + sub + lkey;    // key inside the group
+      const bool live = j < lead.group_len_k;
+      const SeqMeta& m = lead;
       float kk[kDPT], vv[kDPT], dk[kDPT], dv[kDPT];
 #pragma unroll
       for (int e = 0; e < kDPT; ++e) kk[e] = vv[e] = dk[e] = dv[e] = 0.f;
@@ -217,51 +221,56 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(BwdParams p) {
             vv[e] = to_f32(vrow[dbase + e]);
           }
       }
-      // query rows that see any key of this pass: j - shift <= i <= j - lo_shift
-      const int64_t j_first = (int64_t)pr.row0 + sub;
-      const int64_t j_last = min64((int64_t)m.len_k, j_first + KEYS) - 1;
-      const int i_lo = (int)min64((int64_t)m.len_q, max64(0, j_first - (int64_t)m.shift));
-      const int i_hi = (int)max64((int64_t)i_lo, min64((int64_t)m.len_q, j_last - (int64_t)m.lo_shift + 1));
-      for (int h = g * group; h < (g + 1) * group; ++h) {
-        for (int i0 = i_lo; i0 < i_hi; i0 += kRB) {
-          for (int idx = tid; idx < kRB * DMAX; idx += kThreads) {
-            const int ii = idx / DMAX, e = idx % DMAX;
-            const int i = i0 + ii;
-            float qv = 0.f, gv = 0.f;
-            if (i < i_hi && e < d) {
-              qv = to_f32(Q[(int64_t)(m.off_q + i) * p.stride_tok[0] + (int64_t)h * p.stride_head[0] + e]);
-              gv = to_f32(G[(int64_t)(m.off_o + i) * p.stride_tok[4] + (int64_t)h * p.stride_head[4] + e]);
+      for (int mb = pr.b; mb < pr.b + n_mem; ++mb) {   // members of the key group
+        const SeqMeta mm = p.meta[mb];
+        const int64_t j_first = (int64_t)pr.row0 + sub;
+        if (mm.bad != 0 || j_first >= mm.len_k) continue;   // uniform across the block
+        const bool live_m = live && j < mm.len_k;
+        // query rows that see any key of this pass: j - shift <= i <= j - lo_shift
+        const int64_t j_last = min64((int64_t)mm.len_k, j_first + KEYS) - 1;
+        const int i_lo = (int)min64((int64_t)mm.len_q, max64(0, j_first - (int64_t)mm.shift));
+        const int i_hi = (int)max64((int64_t)i_lo, min64((int64_t)mm.len_q, j_last - (int64_t)mm.lo_shift + 1));
+        for (int h = g * group; h < (g + 1) * group; ++h) {
+          for (int i0 = i_lo; i0 < i_hi; i0 += kRB) {
+            for (int idx = tid; idx < kRB * DMAX; idx += kThreads) {
+              const int ii = idx / DMAX, e = idx % DMAX;
+              const int i = i0 + ii;
+              float qv = 0.f, gv = 0.f;
+              if (i < i_hi && e < d) {
+                qv = to_f32(Q[(int64_t)(mm.off_q + i) * p.stride_tok[0] + (int64_t)h * p.stride_head[0] + e]);
+                gv = to_f32(G[(int64_t)(mm.off_o + i) * p.stride_tok[4] + (int64_t)h * p.stride_head[4] + e]);
+              }
+              qs[ii][e] = qv;
+              gs[ii][e] = gv;
             }
-            qs[ii][e] = qv;
-            gs[ii][e] = gv;
-          }
-          if (tid < kRB) {
-            const int i = i0 + tid;
-            lds[tid] = i < i_hi ? p.ld[ld_index(p.pair_base_q, pr.b, i, h, p.h_q)] : make_float2(INFINITY, 0.f);
-          }
-          __syncthreads();
-#pragma unroll 4
-          for (int ii = 0; ii < kRB; ++ii) {
-            float s = 0.f, dp = 0.f;
-#pragma unroll
-            for (int e = 0; e < kDPT; ++e) {
-              s = fmaf(kk[e], qs[ii][dbase + e], s);
-              dp = fmaf(vv[e], gs[ii][dbase + e], dp);
+            if (tid < kRB) {
+              const int i = i0 + tid;
+              lds[tid] = i < i_hi ? p.ld[ld_index(p.pair_base_q, mb, i, h, p.h_q)] : make_float2(INFINITY, 0.f);
             }
-            s = reduce_tpr<TPR>(s);
-            dp = reduce_tpr<TPR>(dp);
-            const int64_t i = (int64_t)i0 + ii;
-            const bool vis = live && i < i_hi && (int64_t)j <= i + m.shift && (int64_t)j >= i + m.lo_shift;
-            const float2 ld = lds[ii];
-            const float pj = vis ? exp2f(s - ld.x) : 0.f;
-            const float ds = pj * (dp - ld.y);
-#pragma unroll
-            for (int e = 0; e < kDPT; ++e) {
-              dv[e] = fmaf(pj, gs[ii][dbase + e], dv[e]);
-              dk[e] = fmaf(ds, qs[ii][dbase + e], dk[e]);
+            __syncthreads();
+  #pragma unroll 4
+            for (int ii = 0; ii < kRB; ++ii) {
+              float s = 0.f, dp = 0.f;
+  #pragma unroll
+              for (int e = 0; e < kDPT; ++e) {
+                s = fmaf(kk[e], qs[ii][dbase + e], s);
+                dp = fmaf(vv[e], gs[ii][dbase + e], dp);
+              }
+              s = reduce_tpr<TPR>(s);
+              dp = reduce_tpr<TPR>(dp);
+              const int64_t i = (int64_t)i0 + ii;
+              const bool vis = live_m && i < i_hi && (int64_t)j <= i + mm.shift && (int64_t)j >= i + mm.lo_shift;
+              const float2 ld = lds[ii];
+              const float pj = vis ? exp2f(s - ld.x) : 0.f;
+              const float ds = pj * (dp - ld.y);
+  #pragma unroll
+              for (int e = 0; e < kDPT; ++e) {
+                dv[e] = fmaf(pj, gs[ii][dbase + e], dv[e]);
+                dk[e] = fmaf(ds, qs[ii][dbase + e], dk[e]);
+              }
             }
+            __syncthreads();
           }
-          __syncthreads();
         }
       }
       if (live) {

@@ -109,9 +109,10 @@ struct BwUnit {
   int32_t n_valid;     // valid rows (dQ) / keys (dK/dV) of the tile
   int32_t t_lo;        // first KV tile (dQ) / first query tile (dK/dV)
   int32_t n_t;         // KV tiles (dQ) / query tiles per head (dK/dV)
-  int32_t n_steps;     // dQ: n_t; dK/dV: n_t x heads of the group
+  int32_t n_steps;     // dQ: n_t; dK/dV: query tiles x heads of the kv group, over every member
   int32_t pb;          // pair_base_q[b]: (LSE2, D) block of the sequence's first query tile
-  int32_t pad[2];
+  int32_t n_mem;       // dK/dV: sequences of the key group (b, b + 1, ...); 1 for dQ
+  int32_t pad;
 };
 static_assert(sizeof(BwUnit) == 80, "BwUnit is 80 bytes");
 
@@ -122,7 +123,8 @@ __device__ __forceinline__ BwUnit empty_unit(uint32_t w) {
   u.len_q = u.len_k = u.shift = u.lo_shift = 0;
   u.off_q = u.off_k = u.off_v = u.off_o = 0;
   u.n_valid = u.t_lo = u.n_t = u.n_steps = u.pb = 0;
-  u.pad[0] = u.pad[1] = 0;
+  u.n_mem = 1;
+  u.pad = 0;
   return u;
 }
 
@@ -156,8 +158,25 @@ __device__ __forceinline__ BwUnit make_unit_dq(const BwdParams& p, uint32_t w, u
   return u;
 }
 
-// dK/dV unit: keys [k0, k0 + 128) of one kv head; for every query head of the
-// group, the query tiles holding rows k0 - shift ... k_last - lo_shift
+// query tiles [t0, t0 + n) of sequence m that see any key of [k0, k0 + 128):
+// key j (< len_k) is seen by rows j - shift <= i <= j - lo_shift
+__device__ __forceinline__ void key_block_tiles(const SeqMeta& m, int k0, int& t0, int& n) {
+  t0 = 0;
+  n = 0;
+  const int keys = max(0, min(BT, m.len_k - k0));
+  if (m.bad != 0 || keys == 0) return;
+  const int64_t i_lo = max64(0, (int64_t)k0 - m.shift);
+  const int64_t i_hi = min64((int64_t)m.len_q, (int64_t)k0 + keys - 1 - m.lo_shift + 1);
+  if (i_hi > i_lo) {
+    t0 = (int)(i_lo / BT);
+    n = (int)((i_hi + BT - 1) / BT) - t0;
+  }
+}
+
+// dK/dV unit: keys [k0, k0 + 128) of one kv head of a key group (the consecutive
+// sequences b .. b + n_mem - 1 that read the same K/V rows; usually one); for every
+// member and every query head of the kv group, the member's query tiles that see
+// those keys. The gradients of all of them accumulate in the unit's TMEM.
 __device__ __forceinline__ BwUnit make_unit_dkdv(const BwdParams& p, uint32_t w, uint32_t num_tiles) {
   BwUnit u = empty_unit(w);
   if (w >= num_tiles) return u;
@@ -168,21 +187,49 @@ __device__ __forceinline__ BwUnit make_unit_dkdv(const BwdParams& p, uint32_t w,
   const int group = p.h_q / p.h_kv;
   u.b = pr.b; u.first = pr.row0; u.g = g; u.h = g * group;
   fill_seq(u, m);
-  const int keys = max(0, min(BT, m.len_k - pr.row0));
-  u.n_valid = keys;
-  int n = 0, t0 = 0;
-  if (keys > 0) {
-    const int64_t i_lo = max64(0, (int64_t)pr.row0 - m.shift);
-    const int64_t i_hi = min64((int64_t)m.len_q, (int64_t)pr.row0 + keys - 1 - m.lo_shift + 1);
-    if (i_hi > i_lo) {
-      t0 = (int)(i_lo / BT);
-      n = (int)((i_hi + BT - 1) / BT) - t0;
-    }
+  u.n_mem = max(1, m.group_n);
+  u.n_valid = max(0, min(BT, m.group_len_k - pr.row0));
+  int steps = 0;
+  for (int e = pr.b; e < pr.b + u.n_mem; ++e) {
+    int t0, n;
+    key_block_tiles(p.meta[e], pr.row0, t0, n);
+    steps += n * group;
   }
-  u.t_lo = t0; u.n_t = n; u.n_steps = n * group;
-  u.pb = p.pair_base_q[pr.b];
+  u.n_steps = steps;
   return u;
 }
+
+// Walks the steps of a dK/dV unit in order: member by member, then query head,
+// then query tile. Every role of the kernel walks the same sequence of steps.
+struct StepCursor {
+  int e, e_end;        // current member, end of the group
+  int t0, nt;          // the member's query tiles
+  int i, n;            // step inside the member, steps of the member
+  int h, t;            // query head and query tile of the current step
+  int pb;              // pair_base_q of the member
+  SeqMeta m;
+  __device__ __forceinline__ void begin(const BwUnit& u) {
+    e = u.b - 1;
+    e_end = u.b + u.n_mem;
+    i = n = 0;
+  }
+  // move to the next step (call once before each step of the unit)
+  __device__ __forceinline__ void next(const BwdParams& p, const BwUnit& u, int group) {
+    while (i >= n && e + 1 < e_end) {
+      ++e;
+      m = p.meta[e];
+      key_block_tiles(m, u.first, t0, nt);
+      n = nt * group;
+      i = 0;
+      pb = p.pair_base_q[e];
+    }
+    if (nt > 0) {
+      h = u.h + i / nt;
+      t = t0 + i % nt;
+    }
+    ++i;
+  }
+};
 
 template <bool BF16>
 __device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
@@ -572,6 +619,7 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t num_tiles = p.header_k[kHdrNumTiles];
+  const int group = p.h_q / p.h_kv;   // query heads per kv head
 
   if (threadIdx.x == 0) {
     init_barriers<C::kStages>(sy);
@@ -618,9 +666,12 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
                            hf * 64, u.g, u.off_v + u.first);
         }
         bool ok = true;
+        StepCursor cur;
+        cur.begin(u);
         for (int i = 0; i < u.n_steps && ok; ++i) {
-          const int h = u.h + i / u.n_t;
-          const int t = u.t_lo + i % u.n_t;
+          cur.next(p, u, group);
+          const int h = cur.h;
+          const int t = cur.t;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {     // 0: Q_i with its (LSE2, D) block, 1: dO_i
             const int st = ring.stage(fill);
@@ -629,12 +680,12 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
             const uint32_t fb = sy.bar(B_RING + st);
             ptx::mbar_arrive_expect_tx(fb, C::kTileBytes + (x == 0 ? C::kLdBytes : 0));
             const void* map = x == 0 ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_do);
-            const int row = (x == 0 ? u.off_q : u.off_o) + t * BT;
+            const int row = (x == 0 ? cur.m.off_q : cur.m.off_o) + t * BT;
 #pragma unroll
             for (int hf = 0; hf < C::kHalves; ++hf)
               ptx::tma_load_3d(sbase + C::kOffRing + st * C::kTileBytes + hf * BT * 128, map, fb, hf * 64, h, row);
             if (x == 0)
-              ptx::bulk_load(sbase + C::kOffLd + st * C::kLdBytes, p.ld + ((int64_t)(u.pb + t) * p.h_q + h) * BT,
+              ptx::bulk_load(sbase + C::kOffLd + st * C::kLdBytes, p.ld + ((int64_t)(cur.pb + t) * p.h_q + h) * BT,
                              C::kLdBytes, fb);
           }
         }
@@ -684,12 +735,14 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
         ptx::tc_commit(sy.bar(B_DP_FULL));
         if (n == 1) ptx::tc_commit(sy.bar(B_IN_EMPTY));
         issued_any = true;
+        StepCursor cur;
+        cur.begin(u);
         for (int i = 0; i < n && ok; ++i) {
           const uint32_t qf = base + 2u * i, of = qf + 1u, qf1 = qf + 2u, of1 = qf + 3u;
           // query rows of this tile past len_q: dV and dK run over ceil(valid/16)
           // steps of 16 rows and the at most 15 rows between are zeroed in Q_i / dO_i
-          const int t = u.t_lo + i % u.n_t;
-          const int valid = min(BT, u.len_q - t * BT);
+          cur.next(p, u, group);
+          const int valid = min(BT, cur.m.len_q - cur.t * BT);
           const int nk = (valid + 15) >> 4;
           const int zr = nk * 16 - valid;
           if (!(ok = sy.wait(B_P_DONE, (p_waits++) & 1u))) break;
@@ -763,17 +816,22 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
       if (lane == 0) ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
       if (u.w >= num_tiles) break;
       const int64_t j = (int64_t)u.first + row;     // key inside the sequence
-      const bool live = row < u.n_valid;
-      // visible query rows of this key: j - shift <= i <= j - lo_shift, i < len_q
-      const int64_t i_min = j - u.shift;
-      const int64_t i_end = min64((int64_t)u.len_q, j - (int64_t)u.lo_shift + 1);
+      const bool live = row < u.n_valid;            // key of the group
       bool ok = true;
+      StepCursor cur;
+      cur.begin(u);
       for (int i = 0; i < u.n_steps; ++i) {
         const uint32_t qf = base + 2u * i;
-        const int t = u.t_lo + i % u.n_t;
+        cur.next(p, u, group);
+        // visible query rows of this key for the step's member: j < len_k and
+        // j - shift <= i <= j - lo_shift, i < len_q
+        const bool live_m = live && j < cur.m.len_k;
+        const int64_t i_min = j - cur.m.shift;
+        const int64_t i_end = min64((int64_t)cur.m.len_q, j - (int64_t)cur.m.lo_shift + 1);
+        const int t = cur.t;
         const int64_t cb = (int64_t)t * BT + wg * 64;     // query row of column 0 of this half
-        const int c_lo = live ? (int)max64(0, min64(64, i_min - cb)) : 64;
-        const int c_hi = live ? (int)max64(0, min64(64, i_end - cb)) : 0;
+        const int c_lo = live_m ? (int)max64(0, min64(64, i_min - cb)) : 64;
+        const int c_hi = live_m ? (int)max64(0, min64(64, i_end - cb)) : 0;
         const float2* lds = reinterpret_cast<const float2*>(smem + C::kOffLd + ring.stage(qf) * C::kLdBytes) + wg * 64;
         if (!(ok = sy.wait_warp(B_S_FULL, (s_cnt++) & 1u))) break;
         // the (LSE2, D) block arrived with Q_i on this stage's barrier

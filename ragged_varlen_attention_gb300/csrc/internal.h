@@ -36,9 +36,13 @@ constexpr int kMaxSmsForSizing = 160;
 // Per-sequence record written by the setup kernel. `shift` is the causal shift:
 // query row i sees keys j < len_k with j <= i + shift (mask 0 stores len_k, which
 // lets every key through for any i >= 0); `lo_shift` the window's lower end:
-// also j >= i + lo_shift (kNoLowerBound when unbounded).
+// also j >= i + lo_shift (kNoLowerBound when unbounded). The last three words are
+// written by the backward's key-axis setup only (zero elsewhere): the key group's
+// member count (0 for a member that is not the group's first sequence), the
+// group's key length (longest valid member), and the sequence's status bits.
 struct SeqMeta {
-  int32_t len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift, lo_shift, pad[3];
+  int32_t len_q, len_k, off_q, off_k, off_v, off_o, off_s, shift, lo_shift;
+  int32_t group_n, group_len_k, bad;
 };
 static_assert(sizeof(SeqMeta) == 48, "SeqMeta is 48 bytes");
 constexpr int32_t kNoLowerBound = -(1 << 30);
@@ -86,6 +90,11 @@ struct SetupParams {
   int64_t tok_stride[5];    // Q K V O Stats token strides (elements), for element offsets
   int32_t num_ctas;         // persistent CTAs of the attention kernel
   int32_t max_split;        // capacity of the split-pair table
+  // key axis of the backward: consecutive sequences with the same K and V offsets
+  // read the same key rows (zigzag context-parallel chunks of one document) and
+  // form one group whose dK/dV units sum over all of its members; K/V rows of
+  // different groups must not overlap (THD_DEV_KEY_OVERLAP otherwise)
+  int32_t group_keys = 0;
   uint32_t* header;
   SeqMeta* meta;
   int32_t* pair_base;       // [batch + 1]

@@ -18,6 +18,12 @@
 // It also zeroes the persistent scheduler's tile counter (header word 0) and
 // writes the status word, pair count and tile count. Invalid sequences get no
 // tiles and set a status bit; their rows are never touched.
+// On the backward's key axis (units over keys for dK/dV), consecutive sequences
+// that read the same K and V rows -- the zigzag query chunks of one document under
+// context parallelism (Megatron-LM PR #14, the packed-CP paths) -- form one key
+// group: its units cover the group's keys and sum the gradient of every member,
+// and key rows shared in any other way are reported (THD_DEV_KEY_OVERLAP) instead
+// of racing.
 #include "internal.h"
 
 namespace thd {
@@ -73,9 +79,47 @@ __device__ __forceinline__ int32_t key_pair_cost(const SeqMeta& m, int32_t k0, i
   return (int32_t)((i_hi + rows_per_tile - 1) / rows_per_tile - i_lo / rows_per_tile);
 }
 
-__device__ __forceinline__ int32_t pair_cost(const SetupParams& p, const SeqMeta& m, int32_t row0) {
-  return p.key_axis ? key_pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile)
-                    : query_pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile);
+// cost of the unit whose pair starts at row0 of sequence b; with key groups the
+// query tiles of every valid member of b's group
+__device__ __forceinline__ int32_t pair_cost(const SetupParams& p, int32_t b, int32_t row0) {
+  const SeqMeta m = p.meta[b];
+  if (!p.key_axis) return query_pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile);
+  if (!p.group_keys) return key_pair_cost(m, row0, p.rows_per_unit, p.keys_per_tile);
+  int32_t c = 0;
+  for (int32_t e = b; e < b + m.group_n; ++e) {
+    const SeqMeta me = p.meta[e];
+    if (me.bad == 0) c += key_pair_cost(me, row0, p.rows_per_unit, p.keys_per_tile);
+  }
+  return c;
+}
+
+__device__ __forceinline__ int64_t block_inclusive_max(int64_t x, int64_t* warp_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = max64(x, y);
+  }
+  if (lane == 31) warp_max[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t s = warp_max[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s = max64(s, y);
+    }
+    warp_max[lane] = s;
+  }
+  __syncthreads();
+  const int64_t r = warp > 0 ? max64(x, warp_max[warp - 1]) : x;
+  __syncthreads();
+  return r;
+}
+
+// sequence e reads the same K and V rows as sequence e - 1
+__device__ __forceinline__ bool same_keys(const SetupParams& p, int32_t e) {
+  return e > 0 && p.off_k[e] == p.off_k[e - 1] && p.off_v[e] == p.off_v[e - 1];
 }
 
 // group of a (clamped) cost: 0 for 512..1023, 1 for 256..511, ..., 9 for 1, 10 for 0
@@ -153,7 +197,9 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
       lo = max64(kNoLowerBound, min64(1ll << 30, lo));
       m.shift = (int32_t)shift;
       m.lo_shift = (int32_t)lo;
-      m.pad[0] = m.pad[1] = m.pad[2] = 0;
+      m.group_n = p.group_keys ? 1 : 0;
+      m.group_len_k = 0;
+      m.bad = p.group_keys ? (int32_t)bad : 0;
       if (bad) {
         atomicOr(&status_s, bad);
         m.len_q = 0;  // no tiles, rows untouched
@@ -166,6 +212,98 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
     if (b < p.batch) p.pair_base[b] = carry + incl - n;
     __syncthreads();
     if (tid == blockDim.x - 1) carry += incl;
+    __syncthreads();
+  }
+  if (p.group_keys) {
+    // 1b. key groups: a run of consecutive sequences with equal K and V offsets is
+    // one group, scheduled from its first member over the longest valid member's
+    // keys; the other members get no pairs of their own
+    __syncthreads();   // every sequence's metadata is written
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int32_t base = 0; base < p.batch; base += blockDim.x) {
+      const int32_t b = base + tid;
+      int32_t n = 0;
+      if (b < p.batch) {
+        SeqMeta* mb = p.meta + b;
+        if (same_keys(p, b)) {
+          mb->group_n = 0;
+        } else {
+          int32_t cnt = 1, glen = mb->bad == 0 ? mb->len_k : 0;
+          for (int32_t e = b + 1; e < p.batch && same_keys(p, e); ++e, ++cnt)
+            if (p.meta[e].bad == 0) glen = max(glen, p.meta[e].len_k);
+          mb->group_n = cnt;
+          mb->group_len_k = glen;
+          n = (glen + p.rows_per_unit - 1) / p.rows_per_unit;
+        }
+      }
+      const int32_t incl = block_inclusive_scan(n, warp_sums);
+      if (b < p.batch) p.pair_base[b] = carry + incl - n;
+      __syncthreads();
+      if (tid == blockDim.x - 1) carry += incl;
+      __syncthreads();
+    }
+    // 1c. the K rows (and the V rows) of different groups must be disjoint: their
+    // dK/dV units would race otherwise. With group starts non-decreasing in batch
+    // order (packed layouts), a group overlaps an earlier one exactly when it starts
+    // before the largest end seen so far; otherwise every pair of groups is checked.
+    __shared__ int64_t warp_max[32];
+    __shared__ int64_t run_start[2], run_end[2];
+    __shared__ int unsorted;
+    if (tid == 0) { run_start[0] = run_start[1] = run_end[0] = run_end[1] = INT64_MIN; unsorted = 0; }
+    __syncthreads();
+    uint32_t overlap = 0;
+    for (int32_t base = 0; base < p.batch; base += blockDim.x) {
+      const int32_t b = base + tid;
+      bool lead = false;
+      SeqMeta m;
+      if (b < p.batch) {
+        m = p.meta[b];
+        lead = m.group_n > 0 && m.group_len_k > 0;
+      }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int64_t st = lead ? (int64_t)(x == 0 ? m.off_k : m.off_v) : INT64_MIN;
+        const int64_t en = lead ? st + m.group_len_k : INT64_MIN;
+        const int64_t max_st = block_inclusive_max(st, warp_max);
+        const int64_t max_en_incl = block_inclusive_max(en, warp_max);
+        // exclusive maxima: shift by one thread through shared memory
+        __shared__ int64_t ex_st[kSetupThreads], ex_en[kSetupThreads];
+        ex_st[tid] = max_st;
+        ex_en[tid] = max_en_incl;
+        __syncthreads();
+        const int64_t prev_st = max64(run_start[x], tid > 0 ? ex_st[tid - 1] : INT64_MIN);
+        const int64_t prev_en = max64(run_end[x], tid > 0 ? ex_en[tid - 1] : INT64_MIN);
+        if (lead) {
+          if (st < prev_st) unsorted = 1;
+          else if (st < prev_en) overlap = 1;
+        }
+        __syncthreads();
+        if (tid == blockDim.x - 1) {
+          run_start[x] = max64(run_start[x], max_st);
+          run_end[x] = max64(run_end[x], max_en_incl);
+        }
+        __syncthreads();
+      }
+    }
+    if (unsorted) {
+      for (int32_t b = tid; b < p.batch; b += blockDim.x) {
+        const SeqMeta m = p.meta[b];
+        if (m.group_n == 0 || m.group_len_k == 0) continue;
+        for (int32_t e = b + 1; e < p.batch && !overlap; ++e) {
+          const SeqMeta o = p.meta[e];
+          if (o.group_n == 0 || o.group_len_k == 0) continue;
+          const bool k_ov = (int64_t)m.off_k < (int64_t)o.off_k + o.group_len_k &&
+                            (int64_t)o.off_k < (int64_t)m.off_k + m.group_len_k;
+          const bool v_ov = (int64_t)m.off_v < (int64_t)o.off_v + o.group_len_k &&
+                            (int64_t)o.off_v < (int64_t)m.off_v + m.group_len_k;
+          if (k_ov || v_ov) overlap = 1;
+        }
+      }
+    }
+    if (overlap) atomicOr(&status_s, (uint32_t)THD_DEV_KEY_OVERLAP);
+    __syncthreads();
+    if (status_s & THD_DEV_KEY_OVERLAP) carry = 0;   // no dK/dV units at all
     __syncthreads();
   }
   int32_t total = carry;
@@ -181,7 +319,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    if (pair_cost(p, p.meta[b], row0) >= kMinSplitCost) atomicAdd(&n_splittable, 1u);
+    if (pair_cost(p, b, row0) >= kMinSplitCost) atomicAdd(&n_splittable, 1u);
   }
   __syncthreads();
   if (tid == 0) {
@@ -196,7 +334,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    const int32_t cost = pair_cost(p, p.meta[b], row0);
+    const int32_t cost = pair_cost(p, b, row0);
     if (split_on && cost >= kMinSplitCost) {
       const int32_t c0 = min(cost / 2, kCostBins - 1), c1 = min(cost - cost / 2, kCostBins - 1);
       atomicAdd(&hist[c0], 1u);
@@ -224,7 +362,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
-    const int32_t cost = pair_cost(p, p.meta[b], row0);
+    const int32_t cost = pair_cost(p, b, row0);
     if (split_on && cost >= kMinSplitCost) {
       const int32_t part = (int32_t)atomicAdd(&n_split_done, 1u);
       SplitRec sr;

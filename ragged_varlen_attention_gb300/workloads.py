@@ -39,7 +39,7 @@ SENTINEL_BYTE = 0xA5
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
 
-WORKLOAD_SEEDS = {"tiny_padded": 101, "padded_causal": 102, "mixed_gqa": 103,
+WORKLOAD_SEEDS = {"tiny_padded": 101, "padded_causal": 102, "mixed_gqa": 103, "zigzag_chunks": 108,
                   "cp_chunks": 104, "separate_padding": 105}
 
 
@@ -219,9 +219,38 @@ def separate_padding(seed: int = WORKLOAD_SEEDS["separate_padding"], b: int = 64
                     q, k, v, cap_q, cap_q)
 
 
+def zigzag_chunks(seed: int = WORKLOAD_SEEDS["zigzag_chunks"], docs: int = 2, doc_len: int = 4096, cp_size: int = 2, ranks=(0, 1),
+                  h_q: int = 4, h_kv: int = 2, d: int = 128, dtype: str = "bf16",
+                  stats_layout: int = STATS_TOKEN_MAJOR) -> ThdBatch:
+    """Zigzag context-parallel query chunks as attention segments (Megatron-LM PR
+    #14, the packed-CP paths): each document is cut into 2 * cp_size chunks of
+    doc_len / (2 * cp_size) rows and rank r holds chunks r and 2 * cp_size - 1 - r.
+    Every chunk is one THD segment whose queries see the key prefix ending with the
+    chunk, bottom-right aligned at q_causal_offset = the chunk's first row in the
+    document. The segments of one document read the SAME K/V rows (equal off_k and
+    off_v, adjacent in the batch), so their key ranges overlap and their dK / dV
+    add up; documents have K/V rows of their own."""
+    rng = np.random.default_rng(seed)
+    c = doc_len // (2 * cp_size)
+    chunks = [ch for r in ranks for ch in (r, 2 * cp_size - 1 - r)]
+    lq = np.full(docs * len(chunks), c, dtype=np.int64)
+    lk = np.array([(ch + 1) * c for _ in range(docs) for ch in chunks], dtype=np.int64)
+    off_q = _cumsum0(lq)
+    off_k = np.repeat(np.arange(docs, dtype=np.int64) * doc_len, len(chunks)).astype(np.int32)
+    off_k = np.concatenate([off_k, [docs * doc_len]]).astype(np.int32)
+    cap_q = int(lq.sum())
+    q = _normal(rng, (cap_q, h_q, d), dtype)
+    k = _normal(rng, (docs * doc_len, h_kv, d), dtype)
+    v = _normal(rng, (docs * doc_len, h_kv, d), dtype)
+    qco = np.array([ch * c for _ in range(docs) for ch in chunks], dtype=np.int32)
+    return ThdBatch("zigzag_chunks", dtype, h_q, h_kv, d, _cumsum0(lq), _cumsum0(lk), off_q, off_k,
+                    off_k.copy(), off_q.copy(), off_q.copy(),
+                    np.full(len(lq), MASK_BOTTOM_RIGHT, dtype=np.int8), qco, stats_layout, q, k, v, cap_q, cap_q)
+
+
 WORKLOADS = {"tiny_padded": tiny_padded, "padded_causal": padded_causal,
              "mixed_gqa": mixed_gqa, "cp_chunks": cp_chunks,
-             "separate_padding": separate_padding}
+             "separate_padding": separate_padding, "zigzag_chunks": zigzag_chunks}
 
 
 def make(name: str, seed: int | None = None, **kw) -> ThdBatch:

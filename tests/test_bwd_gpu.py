@@ -391,3 +391,75 @@ def test_bwd_full_size_sampled(name):
         a, r = res[key][w].float(), alt[key][w].float()
         err = float((a - r).abs().max()) / max(1.0, float(r.abs().max()))
         assert err <= 2 * TOL[batch.dtype], f"{key}: tcgen05 vs SIMT normalised error {err}"
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("d,h_q,h_kv", [(128, 4, 2), (64, 2, 2)])
+def test_bwd_zigzag_chunks_share_keys(kernel, d, h_q, h_kv):
+    """The zigzag query chunks of two documents (Megatron-LM PR #14: under context
+    parallelism rank r holds chunks r and 2*cp-1-r of each document): four segments
+    per document read the SAME K/V rows, each bottom-right over the key prefix that
+    ends with its chunk. dK / dV of a shared row is the sum over the segments that
+    see it, written once; against the oracle, which sums them."""
+    batch = wl.zigzag_chunks(docs=2, doc_len=2048, h_q=h_q, h_kv=h_kv, d=d)
+    res = run_bwd(batch, kernel=kernel, seed=31)
+    assert res["status"] == 0
+    if kernel == bd.KERNEL_AUTO:
+        assert res["plan"].kernel == bd.KERNEL_TCGEN05
+    check_bwd(batch, res)
+
+
+def _shifted_k(batch: wl.ThdBatch, order=None, shift=None):
+    """The batch with its K/V rows laid out per ``order`` (a permutation of the
+    sequences, packed with one gap row) and sequence ``shift[0]`` moved by
+    ``shift[1]`` rows (into its neighbour's rows when that is negative)."""
+    lk = batch.lens_k()
+    order = list(range(batch.batch)) if order is None else order
+    off = np.zeros(batch.batch + 1, dtype=np.int64)
+    pos = 0
+    for b in order:
+        off[b] = pos
+        pos += int(lk[b]) + 1
+    off[batch.batch] = pos
+    if shift is not None:
+        off[shift[0]] += shift[1]
+    k = torch.zeros((pos, batch.h_kv, batch.d), dtype=batch.torch_dtype)
+    v = torch.zeros_like(k)
+    for b in range(batch.batch):
+        n = int(lk[b])
+        k[off[b]:off[b] + n] = batch.k[batch.off_k[b]:batch.off_k[b] + n]
+        v[off[b]:off[b] + n] = batch.v[batch.off_v[b]:batch.off_v[b] + n]
+    off = off.astype(np.int32)
+    return dataclasses.replace(batch, k=k, v=v, off_k=off, off_v=off.copy())
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bwd_unsorted_key_rows(kernel):
+    """Key rows laid out in reverse sequence order (disjoint): the overlap check
+    compares every pair of sequences and finds nothing; gradients exact."""
+    batch = wl.random_pack(7300, batch=5, max_len=200, h_q=2, h_kv=1, d=64, dtype="bf16", allow_empty=False)
+    batch = _shifted_k(batch, order=list(range(batch.batch))[::-1])
+    res = run_bwd(batch, kernel=kernel, seed=32)
+    assert res["status"] == 0
+    check_bwd(batch, res)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("unsorted", [False, True])
+def test_bwd_partial_key_overlap_flagged(kernel, unsorted):
+    """Two sequences whose K/V rows partly overlap without being one key group: the
+    status word reports THD_DEV_KEY_OVERLAP, no dK / dV row is written, dQ is
+    still exact."""
+    batch = wl.random_pack(7301, batch=4, max_len=200, h_q=2, h_kv=1, d=64, dtype="bf16", allow_empty=False)
+    order = [3, 2, 1, 0] if unsorted else None
+    # sequence 2 starts 5 rows before its own rows: inside sequence 1's (or, in
+    # reverse order, sequence 3's) last rows
+    batch = _shifted_k(batch, order=order, shift=(2, -5))
+    res = run_bwd(batch, kernel=kernel, seed=33)
+    assert res["status"] & bd.DEV_KEY_OVERLAP
+    dq_r, _, _, wq, _, _ = oracle_bwd(batch, res)
+    g = res["dq"].to(torch.float64).numpy()[wq]
+    err = float(np.max(np.abs(g - dq_r[wq]))) / max(1.0, float(np.max(np.abs(dq_r[wq]))))
+    assert err <= TOL[batch.dtype]
+    for key in ("dkb", "dvb"):
+        assert (res[key].view(torch.uint8).numpy() == SENTINEL).all(), f"{key} written despite the overlap"
