@@ -30,7 +30,7 @@ static_assert((kHdrNumSplit + 1) * 4 <= kHeaderBytes, "header words");
 // range whose partial results are merged afterwards. kMaxSmsForSizing bounds the
 // SM count the workspace is sized for.
 constexpr int kSplitWaves = 4;
-constexpr int kMinSplitCost = 4;
+constexpr int kMinSplitCost = 16;   // each half keeps >= 8 tiles to amortise a unit's fill and epilogue
 constexpr int kMaxSmsForSizing = 160;
 
 // Per-sequence record written by the setup kernel. `shift` is the causal shift:

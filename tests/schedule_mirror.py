@@ -51,7 +51,7 @@ def unit_order(starts, h_q: int, h_kv: int):
 BAD_LENGTH, BAD_OFFSET, BAD_MASK, TILE_OVERFLOW = 1, 2, 4, 8
 
 
-SPLIT_WAVES, MIN_SPLIT_COST = 4, 4
+SPLIT_WAVES, MIN_SPLIT_COST = 4, 16
 
 
 def split_entries(pairs, h_q: int, num_ctas: int, max_split: int, allow_split: bool):

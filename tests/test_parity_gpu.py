@@ -32,7 +32,7 @@ SMALL = {
     "padded_causal": dict(b=4, h=4, min_len=64, max_len=400),
     "mixed_gqa": dict(b=6, median=128, max_len=700, total=1900, h_q=8, h_kv=2),
     "separate_padding": dict(b=6, max_len=500, h=4),
-    "cp_chunks": dict(docs=2, k_len=1024, q_len=384, h=2),
+    "cp_chunks": dict(docs=2, k_len=2048, q_len=384, h=2),   # 16 KV tiles: the key range splits
 }
 
 
@@ -110,6 +110,22 @@ def test_random_packs(seed, kernel):
     gaps = tuple(int(x) for x in rng.integers(0, 4, size=4))
     res = run_thd(batch, kernel=kernel, gaps=gaps)
     assert res["status"] == 0
+    check_parity(batch, res)
+    check_untouched(batch, res)
+
+
+@pytest.mark.parametrize("seed", [2600, 2603, 2602])
+def test_split_ragged_packs(seed):
+    """Few long ragged sequences (under four waves of units, so pairs of 16 or more
+    KV tiles are processed as two halves and merged): partial tiles, mixed masks,
+    causal offsets and both Stats layouts through the split and combine path."""
+    d, dtype = {2600: (128, "bf16"), 2603: (64, "fp16"), 2602: (128, "bf16")}[seed]
+    batch = wl.random_pack(seed, batch=3, max_len=3000, h_q=2, h_kv=1, d=d, dtype=dtype, allow_empty=False)
+    res = run_thd(batch)
+    hdr, _, _, _ = res["plan"].workspace_layout
+    n_split = int(res["ws"].cpu().numpy()[hdr:hdr + 128].view(np.uint32)[16])
+    assert res["status"] == 0
+    assert n_split > 0, "no pair was split"
     check_parity(batch, res)
     check_untouched(batch, res)
 
