@@ -101,19 +101,69 @@ def load_peaks() -> tuple[dict, str]:
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons sampled while the timed region
+    runs: NVML read every 2 ms from a thread (read-only queries), else nvidia-smi
+    every 100 ms."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.lines: list[str] = []
         self.thread = None
+        self.nvml = None
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self.stop_flag = threading.Event()
+        self.t_begin = None
+
+    def _nvml_open(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        dev = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(dev)) != 0:
+            return None
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(dev, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        if reasons is None:
+            return None
+        return lib, dev, reasons
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, dev, reasons = self.nvml
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if lib.nvmlDeviceGetClockInfo(dev, ctypes.c_int(1), ctypes.byref(clk)) == 0 and \
+                    reasons(dev, ctypes.byref(rs)) == 0:
+                self.samples.append((time.perf_counter(), int(clk.value), int(rs.value)))
+            time.sleep(0.002)
 
     def start(self):
+        try:
+            self.nvml = self._nvml_open()
+        except Exception:       # no NVML here: fall back to nvidia-smi
+            self.nvml = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
@@ -129,7 +179,24 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def begin(self):
+        """The timed region starts now: NVML samples before it are not counted."""
+        self.t_begin = time.perf_counter()
+
     def stop(self) -> dict:
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            try:
+                self.nvml[0].nvmlShutdown()
+            except Exception:
+                pass
+            t0 = self.t_begin if self.t_begin is not None else 0.0
+            kept = [(c, r) for t, c, r in self.samples if t >= t0]
+            sm = [c for c, _ in kept]
+            reasons = sorted({name for _, r in kept for bit, name in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(sm), "source": "nvml, 2 ms"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
@@ -155,7 +222,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 100 ms"}
 
 
 def dist_setup(n_gpus: int):
@@ -398,6 +465,7 @@ def main():
     sampler.start()
     time.sleep(0.3)
     barrier(dist, device)
+    sampler.begin()
     step_ms = []
     if flush is None:
         # one event between consecutive steps: the total and each step's duration
@@ -641,6 +709,7 @@ def bench_backward(args, batch, bd, kernel, device, dist, rank, world):
     sampler.start()
     time.sleep(0.3)
     barrier(dist, device)
+    sampler.begin()
     total_ms = 0.0
     if flush is None:
         ev0.record(stream)
@@ -810,6 +879,7 @@ def bench_indexer(args):
     sampler.start()
     time.sleep(0.3)
     barrier(dist, device)
+    sampler.begin()
     ev0.record(stream)
     for _ in range(args.steps):
         step()
