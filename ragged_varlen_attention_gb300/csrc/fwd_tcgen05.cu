@@ -48,6 +48,26 @@
 
 namespace thd {
 
+// Optional timeline of the kernel's hand-offs, compiled only with -DTHD_FWD_TRACE
+// (the library is built without it; ragged_varlen_attention_gb300.profiling.fwd_timeline
+// builds a traced copy): clock64() stamps of the first unit of each CTA, per KV
+// tile j < kTrTiles, for the two softmax warpgroups (role = sub-tile) and the
+// MMA-issuing thread (role 2). Softmax events: 0 before the S wait, 1 S ready,
+// 2 S in registers, 3 P computed, 4 P stored, 5 arrived. Issuer events: 0 loop top,
+// 1 V_j and K_{j+1} ready, 2 / 4 P_0 / P_1 ready, 3 / 5 after batch 0 / 1 and its
+// commits, 6 after the stage releases.
+#ifdef THD_FWD_TRACE
+constexpr int kTrCtas = 160, kTrRoles = 3, kTrTiles = 64, kTrEvents = 8;
+__device__ unsigned long long g_fwd_trace[kTrCtas * kTrRoles * kTrTiles * kTrEvents];
+__device__ __forceinline__ void trace_stamp(int role, int j, int ev, uint32_t unit_it) {
+  if (unit_it == 0 && blockIdx.x < kTrCtas && j >= 0 && j < kTrTiles)
+    g_fwd_trace[((blockIdx.x * kTrRoles + role) * kTrTiles + j) * kTrEvents + ev] = clock64();
+}
+#define THD_TRACE_STAMP(role, j, ev, it) trace_stamp(role, j, ev, it)
+#else
+#define THD_TRACE_STAMP(role, j, ev, it) ((void)0)
+#endif
+
 namespace {
 
 using tc::Sync;
@@ -376,6 +396,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::tc_commit(sy.bar(B_KV + C::kStages + kv_stage(kv_base)));
         issued_any = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
+          THD_TRACE_STAMP(2, j, 0, it);
           const uint32_t vfill = kv_base + 2u * (uint32_t)j + 1u;
           const uint32_t kfill = kv_base + 2u * (uint32_t)(j + 1);
           const int vstage = kv_stage(vfill);
@@ -383,6 +404,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           const bool kmore = j + 1 < n_tiles;
           ok = sy.wait(B_KV + vstage, kv_phase(vfill)) && (!kmore || sy.wait(B_KV + kstage, kv_phase(kfill)));
           if (!ok) break;
+          THD_TRACE_STAMP(2, j, 1, it);
           // keys of this tile that exist: PV runs over ceil(valid/16) steps of 16
           // keys, and the at most 15 rows between valid and that bound are zeroed
           // (pad rows may hold NaN and 0 * NaN = NaN); whole 128-byte rows, so
@@ -409,6 +431,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               ok = sy.wait(B_O_READ + t, (o_read_waits[t]++) & 1u);
             ok = ok && sy.wait(B_P_DONE + t, (p_waits[t]++) & 1u);
             if (!ok) break;
+            THD_TRACE_STAMP(2, j, 2 + 2 * t, it);
             ptx::tc_fence_after();
             issue_pv(t, vstage, j > tl[t], nk);
             if (j + 1 < te[t]) {
@@ -418,6 +441,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             } else {
               ptx::tc_commit(sy.bar(B_O_FULL + t));
             }
+            THD_TRACE_STAMP(2, j, 3 + 2 * t, it);
           }
           if constexpr (WIN) {
 #pragma unroll
@@ -427,6 +451,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           if (!ok) break;
           ptx::tc_commit(sy.bar(B_KV + C::kStages + vstage));
           if (kmore) ptx::tc_commit(sy.bar(B_KV + C::kStages + kstage));
+          THD_TRACE_STAMP(2, j, 6, it);
         }
         kv_base += 2u * (uint32_t)n_tiles;
 #pragma unroll
@@ -487,14 +512,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int jt0 = u.kv_lo + (WIN ? (t ? u.t_lo[1] : u.t_lo[0]) : 0);   // absolute tile of j = 0
       float m = -INFINITY, l = 0.f;
       bool ok = true;
+#ifdef THD_FWD_TRACE
+      const bool tr = (warp & 3) == 0 && lane == 0;
+#define THD_SOFTMAX_STAMP(ev) do { if (tr) THD_TRACE_STAMP(t, j, ev, it); } while (0)
+#else
+#define THD_SOFTMAX_STAMP(ev) ((void)0)
+#endif
       for (int j = 0; j < n; ++j) {
+        THD_SOFTMAX_STAMP(0);
         if (!(ok = sw.wait_warp(B_S_FULL + t, (s_cnt++) & 1u))) break;
         ptx::tc_fence_after();
+        THD_SOFTMAX_STAMP(1);
         uint32_t s[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld(s[c]);
+        THD_SOFTMAX_STAMP(2);
         const int lim = kmax_row - (jt0 + j) * BN;      // columns >= lim are not visible
         if (lim < BN) {
 #pragma unroll
@@ -575,6 +609,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           compute_p(m == -INFINITY ? 0.f : m, rs);
         }
         l = l * alpha + rs;
+        THD_SOFTMAX_STAMP(3);
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // O_t already holds PV of tiles < j (the commit of S_t(j) covered PV_t(j-1))
 #pragma unroll
@@ -588,8 +623,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
         }
         ptx::tmem_wait_st();
+        THD_SOFTMAX_STAMP(4);
         warp_arrive(B_P_DONE + t);               // this warp's rows of P_t(j) (and O_t rescale) stored
+        THD_SOFTMAX_STAMP(5);
       }
+#undef THD_SOFTMAX_STAMP
       if (!ok) break;
       // epilogue: O = O_acc / l on live rows, LSE = (m + log2 l) * ln 2; dead rows 0 / -inf.
       // For half of a split pair the normalised partial O (fp32) and its base-2 LSE
@@ -680,6 +718,18 @@ cudaError_t launch_impl(const FwdParams& p, const thd_attn_desc_t& desc, int max
 }  // namespace
 
 bool tc_kernel_available() { return true; }
+
+#ifdef THD_FWD_TRACE
+// traced builds only: copy / clear the timeline of the last traced launch
+extern "C" int thd_fwd_trace_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_fwd_trace, bytes < sizeof(g_fwd_trace) ? bytes : sizeof(g_fwd_trace));
+}
+extern "C" int thd_fwd_trace_clear() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fwd_trace) != cudaSuccess) return 1;
+  return (int)cudaMemset(p, 0, sizeof(g_fwd_trace));
+}
+#endif
 int tc_grid_size(int num_sms, int max_pairs, int h_q) {
   // entries: at most two per pair (KV split)
   return (int)max64(1, min64((int64_t)num_sms, 2 * (int64_t)max_pairs * h_q));
