@@ -543,21 +543,63 @@ def main():
             h2d += host[name].numel() * host[name].element_size()
     d2h = o_host.numel() * o_host.element_size() + stats_host.numel() * 4
 
-    def e2e_step():
-        for name in ("q", "k", "v", "cu_q", "cu_k", "mask", "qco", "win"):
-            if host[name] is not None:
-                dev[name].copy_(host[name], non_blocking=True)
-        for dt, ht in zip(dev["offs"], host["offs"]):
-            dt.copy_(ht, non_blocking=True)
-        step()
-        o_host.copy_(o, non_blocking=True)
-        stats_host.copy_(stats, non_blocking=True)
+    # end to end, pipelined the way a serving loop runs: two sets of device inputs and
+    # outputs; while step i computes, step i+1's inputs are copied in on one stream and
+    # step i-1's outputs copied out on another. Every step's copies are inside the timed
+    # region, which runs from before the first input copy to after the last output copy.
+    sets = [dict(dev=dev, o=o, stats=stats)]
+    sets.append(dict(dev={k_: (None if v_ is None else ([t.clone() for t in v_] if isinstance(v_, list) else v_.clone()))
+                          for k_, v_ in dev.items()},
+                     o=torch.empty_like(o), stats=torch.empty_like(stats)))
+    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-    e2e_step()
+    def copy_in(b):
+        d = sets[b]["dev"]
+        with torch.cuda.stream(h2d_s):
+            for name in ("q", "k", "v", "cu_q", "cu_k", "mask", "qco", "win"):
+                if host[name] is not None:
+                    d[name].copy_(host[name], non_blocking=True)
+            for dt, ht in zip(d["offs"], host["offs"]):
+                dt.copy_(ht, non_blocking=True)
+
+    def compute(b):
+        d, ob, sb = sets[b]["dev"], sets[b]["o"], sets[b]["stats"]
+        bd.thd_attn_fwd_window(plan, d["q"], d["k"], d["v"], ob, sb, d["cu_q"], d["cu_k"], *d["offs"], d["mask"],
+                               d["qco"], d["win"], ws, stream)
+
+    def copy_out(b):
+        with torch.cuda.stream(d2h_s):
+            o_host.copy_(sets[b]["o"], non_blocking=True)
+            stats_host.copy_(sets[b]["stats"], non_blocking=True)
+
+    def e2e_run(n_steps):
+        ev = lambda: torch.cuda.Event()
+        in_done, comp_done, out_done = [], [], []
+        copy_in(0)
+        in_done.append(ev()); in_done[0].record(h2d_s)
+        for i in range(n_steps):
+            b = i % 2
+            stream.wait_event(in_done[i])
+            if i >= 2:
+                stream.wait_event(out_done[i - 2])      # outputs of this set copied out
+            compute(b)
+            comp_done.append(ev()); comp_done[i].record(stream)
+            if i + 1 < n_steps:
+                if i >= 1:
+                    h2d_s.wait_event(comp_done[i - 1])  # the other set's inputs are free
+                copy_in(1 - b)
+                in_done.append(ev()); in_done[i + 1].record(h2d_s)
+            d2h_s.wait_event(comp_done[i])
+            copy_out(b)
+            out_done.append(ev()); out_done[i].record(d2h_s)
+        stream.wait_event(out_done[-1])
+
+    e2e_run(2)
+    torch.cuda.synchronize(device)
     barrier(dist, device)
     ev0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    h2d_s.wait_stream(stream)
+    e2e_run(args.e2e_steps)
     ev1.record(stream)
     barrier(dist, device)
     e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / args.e2e_steps, device)
@@ -600,7 +642,9 @@ def main():
         "step_ms_median": statistics.median(step_ms) if step_ms else None,
         "graph_replay_ms_per_step": graph_ms,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": args.e2e_steps},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+                "pipeline": "step i+1's inputs copied in and step i-1's outputs copied out on two "
+                            "streams while step i computes (two device buffer sets)"},
         "gpu_launches": (3 if plan.kernel == bd.KERNEL_TCGEN05 and not args.no_kv_split else 2) * args.steps,
         "clocks": clocks,
     }

@@ -40,7 +40,7 @@ SENTINEL_BYTE = 0xA5
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
 
 WORKLOAD_SEEDS = {"tiny_padded": 101, "padded_causal": 102, "mixed_gqa": 103, "zigzag_chunks": 108,
-                  "cp_chunks": 104, "separate_padding": 105}
+                  "cp_chunks": 104, "separate_padding": 105, "cp_chunks_one_doc": 104}
 
 
 @dataclass
@@ -248,9 +248,16 @@ def zigzag_chunks(seed: int = WORKLOAD_SEEDS["zigzag_chunks"], docs: int = 2, do
                     np.full(len(lq), MASK_BOTTOM_RIGHT, dtype=np.int8), qco, stats_layout, q, k, v, cap_q, cap_q)
 
 
+def cp_chunks_one_doc(seed: int = WORKLOAD_SEEDS["cp_chunks"], **kw) -> ThdBatch:
+    """One document of the cp_chunks workload (65536 keys, a 4096-row chunk): the same
+    per-unit work on half the units, for profiler captures that must stay small."""
+    return cp_chunks(seed=seed, docs=1, **kw)
+
+
 WORKLOADS = {"tiny_padded": tiny_padded, "padded_causal": padded_causal,
              "mixed_gqa": mixed_gqa, "cp_chunks": cp_chunks,
-             "separate_padding": separate_padding, "zigzag_chunks": zigzag_chunks}
+             "separate_padding": separate_padding, "zigzag_chunks": zigzag_chunks,
+             "cp_chunks_one_doc": cp_chunks_one_doc}
 
 
 def make(name: str, seed: int | None = None, **kw) -> ThdBatch:
