@@ -189,45 +189,69 @@ __device__ __forceinline__ BwUnit make_unit_dkdv(const BwdParams& p, uint32_t w,
   fill_seq(u, m);
   u.n_mem = max(1, m.group_n);
   u.n_valid = max(0, min(BT, m.group_len_k - pr.row0));
+  // a lone sequence (the common case) keeps its tiles and pair base in the unit, so
+  // the roles walk its steps without reading its metadata again
   int steps = 0;
-  for (int e = pr.b; e < pr.b + u.n_mem; ++e) {
+  key_block_tiles(m, pr.row0, u.t_lo, u.n_t);
+  steps = u.n_t * group;
+  for (int e = pr.b + 1; e < pr.b + u.n_mem; ++e) {
     int t0, n;
     key_block_tiles(p.meta[e], pr.row0, t0, n);
     steps += n * group;
   }
   u.n_steps = steps;
+  u.pb = p.pair_base_q[pr.b];
   return u;
 }
 
 // Walks the steps of a dK/dV unit in order: member by member, then query head,
-// then query tile. Every role of the kernel walks the same sequence of steps.
+// then query tile. Every role of the kernel walks the same sequence of steps; a
+// member's fields are set once per member (`fresh` marks its first step), from the
+// unit itself for its first member and from the metadata for the others.
 struct StepCursor {
   int e, e_end;        // current member, end of the group
-  int t0, nt;          // the member's query tiles
-  int i, n;            // step inside the member, steps of the member
+  int t0, t_end;       // the member's query tiles [t0, t_end)
+  int hh;              // query head offset inside the kv group
   int h, t;            // query head and query tile of the current step
   int pb;              // pair_base_q of the member
-  SeqMeta m;
-  __device__ __forceinline__ void begin(const BwUnit& u) {
+  int len_q, len_k, shift, lo_shift, off_q, off_o;
+  bool fresh;          // this step is the member's first
+  __device__ __forceinline__ void begin(const BwUnit& u, int group) {
     e = u.b - 1;
     e_end = u.b + u.n_mem;
-    i = n = 0;
+    t = t_end = 0;
+    hh = group - 1;
   }
   // move to the next step (call once before each step of the unit)
   __device__ __forceinline__ void next(const BwdParams& p, const BwUnit& u, int group) {
-    while (i >= n && e + 1 < e_end) {
-      ++e;
-      m = p.meta[e];
-      key_block_tiles(m, u.first, t0, nt);
-      n = nt * group;
-      i = 0;
-      pb = p.pair_base_q[e];
+    fresh = false;
+    if (t + 1 < t_end) {
+      ++t;
+    } else if (hh + 1 < group) {
+      ++hh;
+      t = t0;
+    } else {
+      int nt = 0;
+      while (nt == 0 && e + 1 < e_end) {
+        ++e;
+        if (e == u.b) {
+          t0 = u.t_lo; nt = u.n_t; pb = u.pb;
+          len_q = u.len_q; len_k = u.len_k; shift = u.shift; lo_shift = u.lo_shift;
+          off_q = u.off_q; off_o = u.off_o;
+        } else {
+          const SeqMeta m = p.meta[e];
+          key_block_tiles(m, u.first, t0, nt);
+          pb = p.pair_base_q[e];
+          len_q = m.len_q; len_k = m.len_k; shift = m.shift; lo_shift = m.lo_shift;
+          off_q = m.off_q; off_o = m.off_o;
+        }
+      }
+      t_end = t0 + nt;
+      t = t0;
+      hh = 0;
+      fresh = true;
     }
-    if (nt > 0) {
-      h = u.h + i / nt;
-      t = t0 + i % nt;
-    }
-    ++i;
+    h = u.h + hh;
   }
 };
 
@@ -667,7 +691,7 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
         }
         bool ok = true;
         StepCursor cur;
-        cur.begin(u);
+        cur.begin(u, group);
         for (int i = 0; i < u.n_steps && ok; ++i) {
           cur.next(p, u, group);
           const int h = cur.h;
@@ -680,7 +704,7 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
             const uint32_t fb = sy.bar(B_RING + st);
             ptx::mbar_arrive_expect_tx(fb, C::kTileBytes + (x == 0 ? C::kLdBytes : 0));
             const void* map = x == 0 ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_do);
-            const int row = (x == 0 ? cur.m.off_q : cur.m.off_o) + t * BT;
+            const int row = (x == 0 ? cur.off_q : cur.off_o) + t * BT;
 #pragma unroll
             for (int hf = 0; hf < C::kHalves; ++hf)
               ptx::tma_load_3d(sbase + C::kOffRing + st * C::kTileBytes + hf * BT * 128, map, fb, hf * 64, h, row);
@@ -736,13 +760,13 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
         if (n == 1) ptx::tc_commit(sy.bar(B_IN_EMPTY));
         issued_any = true;
         StepCursor cur;
-        cur.begin(u);
+        cur.begin(u, group);
         for (int i = 0; i < n && ok; ++i) {
           const uint32_t qf = base + 2u * i, of = qf + 1u, qf1 = qf + 2u, of1 = qf + 3u;
           // query rows of this tile past len_q: dV and dK run over ceil(valid/16)
           // steps of 16 rows and the at most 15 rows between are zeroed in Q_i / dO_i
           cur.next(p, u, group);
-          const int valid = min(BT, cur.m.len_q - cur.t * BT);
+          const int valid = min(BT, cur.len_q - cur.t * BT);
           const int nk = (valid + 15) >> 4;
           const int zr = nk * 16 - valid;
           if (!(ok = sy.wait(B_P_DONE, (p_waits++) & 1u))) break;
@@ -819,15 +843,19 @@ __global__ void __launch_bounds__(kThreadsBw, 1)
       const bool live = row < u.n_valid;            // key of the group
       bool ok = true;
       StepCursor cur;
-      cur.begin(u);
+      cur.begin(u, group);
+      bool live_m = false;
+      int64_t i_min = 0, i_end = 0;
       for (int i = 0; i < u.n_steps; ++i) {
         const uint32_t qf = base + 2u * i;
         cur.next(p, u, group);
-        // visible query rows of this key for the step's member: j < len_k and
-        // j - shift <= i <= j - lo_shift, i < len_q
-        const bool live_m = live && j < cur.m.len_k;
-        const int64_t i_min = j - cur.m.shift;
-        const int64_t i_end = min64((int64_t)cur.m.len_q, j - (int64_t)cur.m.lo_shift + 1);
+        if (cur.fresh) {
+          // visible query rows of this key for the step's member: j < len_k and
+          // j - shift <= i <= j - lo_shift, i < len_q
+          live_m = live && j < cur.len_k;
+          i_min = j - cur.shift;
+          i_end = min64((int64_t)cur.len_q, j - (int64_t)cur.lo_shift + 1);
+        }
         const int t = cur.t;
         const int64_t cb = (int64_t)t * BT + wg * 64;     // query row of column 0 of this half
         const int c_lo = live_m ? (int)max64(0, min64(64, i_min - cb)) : 64;
