@@ -463,3 +463,24 @@ def test_bwd_partial_key_overlap_flagged(kernel, unsorted):
     assert err <= TOL[batch.dtype]
     for key in ("dkb", "dvb"):
         assert (res[key].view(torch.uint8).numpy() == SENTINEL).all(), f"{key} written despite the overlap"
+
+
+def test_bwd_full_size_every_row_mixed_gqa():
+    """The full-size mixed-policy GQA workload in the benchmark's launch configuration
+    (O and Stats from this library's forward): dQ, dK and dV of every row and head
+    against the backward oracle (normalised max error per gradient, as elsewhere),
+    and every row outside the sequences untouched."""
+    batch = wl.make("mixed_gqa")
+    res = _bwd_after_fwd(batch)
+    assert res["status"] == 0
+    assert res["plan"].kernel == bd.KERNEL_TCGEN05
+    dq_r, dk_r, dv_r, wq, wk, wv = oracle_bwd(batch, res)
+    tol = TOL[batch.dtype]
+    for name, got, ref, w in (("dq", res["dq"], dq_r, wq), ("dk", res["dk"], dk_r, wk), ("dv", res["dv"], dv_r, wv)):
+        g = got.to(torch.float64).numpy()[w]
+        r = ref[w]
+        assert np.isfinite(g).all(), f"non-finite {name}"
+        err = float(np.max(np.abs(g - r))) / max(1.0, float(np.max(np.abs(r))))
+        assert err <= tol, f"{name}: normalised error {err} > {tol}"
+        raw = got.view(torch.uint8).numpy().reshape(got.shape[0], -1)
+        assert (raw[~w] == SENTINEL).all(), f"a row of {name} outside the sequences was written"
