@@ -120,10 +120,11 @@ typedef struct {
 /* Plan flags.
  * THD_FLAG_NO_KV_SPLIT: never split a unit's key range. By default, when a launch
  *   has fewer than about four waves of work units for the GPU, the tensor-core
- *   path processes long units as two halves of their key range and merges the
- *   halves' partial results (log-sum-exp weighted) in a small follow-up kernel,
- *   which evens out the last wave. The partial results live in the workspace, so
- *   splitting enlarges workspace_bytes; this flag keeps the workspace small. */
+ *   path processes long units as two halves of their key range (and the cheapest
+ *   long ones whose units would make up a last, partial wave as eight parts) and
+ *   merges the parts' partial results (log-sum-exp weighted) in a small follow-up
+ *   kernel, which evens out the end of the launch. The partial results live in the
+ *   workspace, so splitting enlarges workspace_bytes; this flag keeps it small. */
 enum { THD_FLAG_NO_KV_SPLIT = 1u << 0 };
 /* THD_FLAG_ELEMENT_OFFSETS: the five offset arrays hold ELEMENT offsets, the
  * convention where a sequence's offset is its first row times the tensor's token
@@ -207,8 +208,9 @@ void thd_attn_plan_geometry(thd_attn_plan_t plan, int32_t* rows_per_unit,
  * split count), [1] per-sequence metadata (12 int32 per sequence: len_q, len_k,
  * off_q, off_k, off_v, off_o, off_s, shift, window lower shift, 3 unused), [2]
  * per-sequence first pair index
- * (int32 [B+1]), [3] the scheduled entry list (int32 {b, first query row, split,
- * partial slot} per entry, longest first). For inspection only. */
+ * (int32 [B+1]), [3] the scheduled entry list (int32 {b, first query row,
+ * (part << 8) | parts, partial slot or -1} per entry, longest first). For
+ * inspection only. */
 void thd_attn_plan_workspace_layout(thd_attn_plan_t plan, int64_t offsets[4]);
 
 void thd_attn_plan_destroy(thd_attn_plan_t plan);

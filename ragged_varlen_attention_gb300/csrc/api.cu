@@ -160,13 +160,24 @@ thd_status_t thd_attn_plan(thd_attn_plan_t* out, const thd_attn_desc_t* desc, si
   p->allow_split = kernel == THD_KERNEL_TCGEN05 && !(d.flags & THD_FLAG_NO_KV_SPLIT);
   const int64_t split_bound = ((int64_t)thd::kSplitWaves * thd::kMaxSmsForSizing + d.h_q - 1) / d.h_q;
   p->max_split = p->allow_split ? (int32_t)(max_pairs < split_bound ? max_pairs : split_bound) : 0;
-  const int64_t part_rows = (int64_t)p->max_split * 2 * d.h_q * p->rows_per_unit;
+  p->max_tail = p->max_split < thd::max_tail_pairs(d.h_q) ? p->max_split : thd::max_tail_pairs(d.h_q);
+  // partial slots: two per split pair, kTailParts per pair cut for the last wave;
+  // the pair list holds every pair plus the extra parts of the split ones
+  const int64_t slots = 2 * (int64_t)p->max_split + (int64_t)(thd::kTailParts - 2) * p->max_tail;
+  const int64_t entries = max_pairs + (p->allow_split ? (int64_t)p->max_split + (thd::kTailParts - 2) * p->max_tail : 0);
+  if (entries * d.h_q >= (int64_t(1) << 31)) {
+    delete p;
+    return THD_ERR_UNSUPPORTED;
+  }
+  p->pair_cap = (int32_t)entries;
+  p->slot_cap = (int32_t)slots;
+  const int64_t part_rows = slots * d.h_q * p->rows_per_unit;
   int64_t off = 0;
   p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
   p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
   p->ws_off[2] = off; off = align_up(off + ((int64_t)d.batch + 1) * 4, kAlign);
   p->ws_off[3] = off;
-  off = align_up(off + (p->allow_split ? 2 : 1) * max_pairs * (int64_t)sizeof(thd::PairRec), kAlign);
+  off = align_up(off + entries * (int64_t)sizeof(thd::PairRec), kAlign);
   p->ws_off[4] = off; off = align_up(off + (int64_t)p->max_split * (int64_t)sizeof(thd::SplitRec), kAlign);
   p->ws_off[5] = off; off = align_up(off + part_rows * d.d * 4, kAlign);
   p->ws_off[6] = off; off = align_up(off + part_rows * 4, kAlign);
@@ -284,6 +295,8 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
   sp.rows_per_unit = plan->rows_per_unit;
   sp.keys_per_tile = plan->keys_per_tile;
   sp.max_pairs = plan->max_pairs;
+  sp.pair_cap = plan->pair_cap > 0 ? plan->pair_cap : plan->max_pairs;
+  sp.slot_cap = plan->slot_cap;
   sp.h_q = d.h_q;
   sp.key_axis = 0;
   sp.max_len_k = 0;
@@ -294,6 +307,7 @@ thd_status_t thd_attn_fwd_window(thd_attn_plan_t plan, const void* q, const void
   for (int i = 0; i < 4; ++i) sp.tok_stride[i] = d.stride_tok[i] > 0 ? d.stride_tok[i] : 1;
   sp.tok_stride[4] = plan->stats_tok > 0 ? plan->stats_tok : 1;
   sp.max_split = plan->max_split;
+  sp.max_tail = plan->max_tail;
   sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
   sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
   sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
@@ -456,6 +470,7 @@ thd_status_t thd_attn_plan_bwd(thd_attn_plan_t* out, const thd_attn_bwd_desc_t* 
   p->max_pairs_k = (int32_t)max_k;
   p->allow_split = 0;
   p->max_split = 0;
+  p->max_tail = 0;
   int64_t off = 0;
   p->ws_off[0] = off; off = align_up(off + thd::kHeaderBytes, kAlign);
   p->ws_off[1] = off; off = align_up(off + (int64_t)d.batch * (int64_t)sizeof(thd::SeqMeta), kAlign);
@@ -523,6 +538,7 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   for (int i = 0; i < 4; ++i) sp.tok_stride[i] = d.stride_tok[i] > 0 ? d.stride_tok[i] : 1;
   sp.tok_stride[4] = plan->stats_tok > 0 ? plan->stats_tok : 1;
   sp.max_split = 0;
+  sp.max_tail = 0;
   sp.num_ctas = num_sms;
   sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
   sp.splits = nullptr;
@@ -532,6 +548,8 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   sp.rows_per_unit = plan->rows_per_unit;
   sp.keys_per_tile = thd::kBwdKeysPerUnit;
   sp.max_pairs = plan->max_pairs;
+  sp.pair_cap = plan->pair_cap > 0 ? plan->pair_cap : plan->max_pairs;
+  sp.slot_cap = plan->slot_cap;
   sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
   sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
   sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off[3]);
@@ -547,6 +565,8 @@ thd_status_t thd_attn_bwd(thd_attn_plan_t plan, const void* q, const void* k, co
   sp.rows_per_unit = thd::kBwdKeysPerUnit;
   sp.keys_per_tile = plan->rows_per_unit;
   sp.max_pairs = plan->max_pairs_k;
+  sp.pair_cap = plan->max_pairs_k;
+  sp.slot_cap = 0;
   sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off_b[0]);
   sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off_b[1]);
   sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off_b[2]);
@@ -688,6 +708,8 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
   sp.rows_per_unit = plan->rows_per_unit;
   sp.keys_per_tile = plan->keys_per_tile;
   sp.max_pairs = plan->max_pairs;
+  sp.pair_cap = plan->pair_cap > 0 ? plan->pair_cap : plan->max_pairs;
+  sp.slot_cap = plan->slot_cap;
   sp.h_q = 1;
   sp.key_axis = 0;
   sp.max_len_k = d.max_seqlen_k;   // 0: len_k <= cap_rows_k <= the score row already
@@ -698,6 +720,7 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
   for (int i = 0; i < 5; ++i) sp.tok_stride[i] = 1;
   sp.num_ctas = num_sms;
   sp.max_split = 0;
+  sp.max_tail = 0;
   sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off[0]);
   sp.meta = reinterpret_cast<thd::SeqMeta*>(ws + plan->ws_off[1]);
   sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off[2]);
@@ -714,6 +737,8 @@ thd_status_t thd_indexer_topk(thd_attn_plan_t plan, const void* q_i, const void*
     sp.rows_per_unit = thd::kIndexerKeysPerUnit;
     sp.keys_per_tile = 128;
     sp.max_pairs = plan->max_pairs_k;
+    sp.pair_cap = plan->max_pairs_k;
+    sp.slot_cap = 0;
     sp.header = reinterpret_cast<uint32_t*>(ws + plan->ws_off_b[1]);
     sp.pair_base = reinterpret_cast<int32_t*>(ws + plan->ws_off_b[2]);
     sp.pairs = reinterpret_cast<thd::PairRec*>(ws + plan->ws_off_b[3]);

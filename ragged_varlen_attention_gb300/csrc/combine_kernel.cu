@@ -1,11 +1,11 @@
-// Merge of split KV ranges: a pair whose key range the setup kernel split in two
-// left, for each half h in {0, 1}, a normalised partial output O_h and a base-2
-// log-sum-exp L_h per (row, head) in the workspace. The row's result is the
-// log-sum-exp weighted combination
-//     M = max(L_0, L_1),  w_h = 2^(L_h - M),  W = w_0 + w_1,
-//     O = (w_0 O_0 + w_1 O_1) / W,  LSE = (M + log2 W) * ln 2,
-// which equals the softmax over the union of the two key ranges; a row with no
-// visible key in either half (both L_h = -inf) gets O = 0 and LSE = -inf. Only
+// Merge of split KV ranges: a pair whose key range the setup kernel cut into n
+// parts (n = 2, or more at the end of a launch) left, for each part i, a normalised
+// partial output O_i and a base-2 log-sum-exp L_i per (row, head) in the
+// workspace. The row's result is the log-sum-exp weighted combination
+//     M = max_i L_i,  w_i = 2^(L_i - M),  W = sum_i w_i,
+//     O = sum_i w_i O_i / W,  LSE = (M + log2 W) * ln 2,
+// which equals the softmax over the union of the key ranges; a row with no
+// visible key in any part (every L_i = -inf) gets O = 0 and LSE = -inf. Only
 // rows r < len_q of each pair are written, at the caller's O and Stats offsets.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -61,19 +61,25 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
     const SeqMeta m = p.meta[sr.b];
     const int r = sr.row0 + urow;
     if (r >= m.len_q) continue;
-    const int64_t base0 = ((int64_t)(2 * part) * p.h_q + h) * p.rows_per_unit + urow;
-    const int64_t base1 = ((int64_t)(2 * part + 1) * p.h_q + h) * p.rows_per_unit + urow;
-    const float l0 = p.part_lse[base0], l1 = p.part_lse[base1];
-    const float4 a = *reinterpret_cast<const float4*>(p.part_o + base0 * p.d + e);
-    const float4 b = *reinterpret_cast<const float4*>(p.part_o + base1 * p.d + e);
-    const float mx = fmaxf(l0, l1);
+    // slot s holds rows [((s h_q + h) rows_per_unit + urow)]
+    auto row_of = [&](int i) { return ((int64_t)(sr.slot0 + i) * p.h_q + h) * p.rows_per_unit + urow; };
+    float mx = -INFINITY;
+    for (int i = 0; i < sr.parts; ++i) mx = fmaxf(mx, p.part_lse[row_of(i)]);
     const bool dead = mx == -INFINITY;
-    const float w0 = dead ? 0.f : exp2f(l0 - mx), w1 = dead ? 0.f : exp2f(l1 - mx);
-    const float wsum = w0 + w1;
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!dead) {
+      for (int i = 0; i < sr.parts; ++i) {
+        const int64_t ri = row_of(i);
+        const float w = exp2f(p.part_lse[ri] - mx);
+        const float4 a = *reinterpret_cast<const float4*>(p.part_o + ri * p.d + e);
+        wsum += w;
+        acc.x += w * a.x; acc.y += w * a.y; acc.z += w * a.z; acc.w += w * a.w;
+      }
+    }
     const float inv = dead ? 0.f : 1.f / wsum;
     T* orow = O + (int64_t)(m.off_o + r) * p.stride_tok[3] + (int64_t)h * p.stride_head[3];
-    store4<T>(orow + e, (w0 * a.x + w1 * b.x) * inv, (w0 * a.y + w1 * b.y) * inv, (w0 * a.z + w1 * b.z) * inv,
-              (w0 * a.w + w1 * b.w) * inv);
+    store4<T>(orow + e, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (e == 0)
       p.stats[(int64_t)(m.off_s + r) * p.stats_tok + (int64_t)h * p.stats_head] =
           dead ? -INFINITY : (mx + log2f(wsum)) * 0.69314718055994530942f;

@@ -64,8 +64,24 @@ __device__ __forceinline__ void trace_stamp(int role, int j, int ev, uint32_t un
     g_fwd_trace[((blockIdx.x * kTrRoles + role) * kTrTiles + j) * kTrEvents + ev] = clock64();
 }
 #define THD_TRACE_STAMP(role, j, ev, it) trace_stamp(role, j, ev, it)
+// per CTA and unit u < kTrUnits, %globaltimer (ns, one clock for all SMs): 0 unit
+// claimed, 1 its loads issued, 2 issuing thread has it, 3 first QK committed, 4 last
+// MMA committed, 5 / 6 epilogue of sub-tile 0 / 1 stored, 7 (work id << 32) | KV tiles.
+// g_fwd_cta: CTA start (after the prologue) and end.
+constexpr int kTrUnits = 16, kTrUEvents = 8;
+__device__ unsigned long long g_fwd_units[kTrCtas * kTrUnits * kTrUEvents];
+__device__ unsigned long long g_fwd_cta[kTrCtas * 2];
+__device__ __forceinline__ void unit_stamp(uint32_t u, int ev, unsigned long long v) {
+  if (blockIdx.x < kTrCtas && u < kTrUnits) g_fwd_units[(blockIdx.x * kTrUnits + u) * kTrUEvents + ev] = v;
+}
+#define THD_UNIT_STAMP(u, ev) unit_stamp(u, ev, ptx::globaltimer_ns())
+#define THD_UNIT_INFO(u, v) unit_stamp(u, 7, v)
+#define THD_CTA_STAMP(ev) do { if (blockIdx.x < kTrCtas) g_fwd_cta[blockIdx.x * 2 + (ev)] = ptx::globaltimer_ns(); } while (0)
 #else
 #define THD_TRACE_STAMP(role, j, ev, it) ((void)0)
+#define THD_UNIT_STAMP(u, ev) ((void)0)
+#define THD_UNIT_INFO(u, v) ((void)0)
+#define THD_CTA_STAMP(ev) ((void)0)
 #endif
 
 namespace {
@@ -101,6 +117,9 @@ struct Cfg {
   static constexpr int kHalves = D / 64;               // 128-byte swizzle atoms along d
   static constexpr int kTileBytes = BN * D * 2;        // a K or V tile; also a Q sub-tile (BM == BN)
   static constexpr int kStages = D == 128 ? 5 : 10;    // K/V ring depth (fills 224 KB with Q)
+  // one barrier for V_j and K_{j+1} (one wait and one release per tile instead of
+  // two): 5 % faster at d = 64, 0.3 % slower at d = 128 (measured A/B), so d = 64 only
+  static constexpr bool kGroupKV = D == 64;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
@@ -122,7 +141,7 @@ struct UnitInfo {
   int32_t n_rows[2];     // valid query rows of each sub-tile
   int32_t kv_lo;         // absolute KV tile of loop index 0
   int32_t n_tiles;       // KV tiles loaded for this entry
-  int32_t part_slot;     // partial-result slot (2 * part + half), -1 for a whole pair
+  int32_t part_slot;     // partial-result slot, -1 for a whole pair
   int32_t pad[2];
 };
 static_assert(sizeof(UnitInfo) == 96, "UnitInfo is 96 bytes");
@@ -165,16 +184,16 @@ __device__ __forceinline__ UnitInfo make_unit(const FwdParams& p, uint32_t w, ui
       end[t] = kmax > 0 ? (int)((kmax + BN - 1) / BN) : 0;
     }
   }
-  // the pair spans [first[0], max end); a split pair covers the lower half of that
-  // span in its first half and the rest in its second
+  // the pair spans n tiles [first[0], max end); part i of a pair split into `parts`
+  // covers [i n / parts, (i + 1) n / parts) of that span
   const int f_pair = first[0];
   const int n_pair = max(0, max(end[0], end[1]) - f_pair);
-  const int halves = pr.split & 0xff, half = pr.split >> 8;
+  const int parts = pr.split & 0xff, part = pr.split >> 8;
   int lo = f_pair, hi = f_pair + n_pair;
-  if (halves == 2) {
-    lo = f_pair + (half == 0 ? 0 : n_pair / 2);
-    hi = f_pair + (half == 0 ? n_pair / 2 : n_pair);
-    u.part_slot = 2 * pr.part + half;
+  if (parts > 1) {
+    lo = f_pair + (int)(((int64_t)part * n_pair) / parts);
+    hi = f_pair + (int)(((int64_t)(part + 1) * n_pair) / parts);
+    u.part_slot = pr.part;
   }
   int start[2], kv_lo = hi;
 #pragma unroll
@@ -211,7 +230,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t num_tiles = p.header[kHdrNumTiles];
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -246,6 +264,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t num_tiles = p.header[kHdrNumTiles];
+  if (threadIdx.x == 0) THD_CTA_STAMP(0);
 
   if (warp >= 8) {
     ptx::setmaxnreg_dec<kRegsControl>();
@@ -253,11 +273,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // ---------------------------------------------- scheduler + TMA producer
       uint32_t q_uses[2] = {0, 0};
       uint32_t kv_it = 0;
+      // per ring slot: ever filled; its last fill released by the empty barrier of the
+      // next slot (else its own); parity of that release phase. Per barrier slot:
+      // parity of the empty phases handed out and of the full phases armed; armed once
+      uint32_t filled = 0, rel_next = 0, rel_par = 0, e_cnt = 0, f_cnt = 0, f_used = 0;
       for (uint32_t it = 0;; ++it) {
         const int slot = (int)(it & 1u);
         if (!sy.wait(B_SCHED_EMPTY + slot, ((it >> 1) & 1u) ^ 1u)) break;
         const uint32_t w = atomicAdd(p.counter, 1u);
         const UnitInfo u = make_unit(p, w, num_tiles);
+        THD_UNIT_STAMP(it, 0);
+        THD_UNIT_INFO(it, ((unsigned long long)w << 32) | (uint32_t)u.n_tiles);
         info[slot] = u;
         ptx::mbar_arrive(sy.bar(B_SCHED_FULL + slot));
         if (w >= num_tiles) break;
@@ -275,33 +301,83 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                              u.off_q + u.row0 + t * BM);
         }
         const int n_tiles = u.n_tiles;
-        for (int j = 0; j < n_tiles && ok; ++j) {
+        if constexpr (!C::kGroupKV) {
+          // one full and one empty barrier per ring slot, K_j then V_j
+          for (int j = 0; j < n_tiles && ok; ++j) {
 #pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            const int stage = (int)(kv_it % C::kStages);
-            if (!(ok = sy.wait(B_KV + C::kStages + stage, ((kv_it / C::kStages) & 1u) ^ 1u))) break;
-            ++kv_it;
-            const uint32_t fbar = sy.bar(B_KV + stage);
-            ptx::mbar_arrive_expect_tx(fbar, C::kTileBytes);
-            const void* map = kv == 0 ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
-            const int row = (kv == 0 ? u.off_k : u.off_v) + (u.kv_lo + j) * BN;
+            for (int kv = 0; kv < 2; ++kv) {
+              const int stage = (int)(kv_it % C::kStages);
+              if (!(ok = sy.wait(B_KV + C::kStages + stage, ((kv_it / C::kStages) & 1u) ^ 1u))) break;
+              ++kv_it;
+              const uint32_t fbar = sy.bar(B_KV + stage);
+              ptx::mbar_arrive_expect_tx(fbar, C::kTileBytes);
+              const void* map = kv == 0 ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+              const int row = (kv == 0 ? u.off_k : u.off_v) + (u.kv_lo + j) * BN;
 #pragma unroll
-            for (int hf = 0; hf < C::kHalves; ++hf)
-              ptx::tma_load_3d(sbase + C::kOffKV + stage * C::kTileBytes + hf * BN * 128, map, fbar, hf * 64, u.g,
-                               row);
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                ptx::tma_load_3d(sbase + C::kOffKV + stage * C::kTileBytes + hf * BN * 128, map, fbar, hf * 64,
+                                 u.g, row);
+            }
+          }
+        } else {
+          // fills i = 0 .. 2n-1 in order K_0, V_0, K_1, ..., V_{n-1} (K_j = 2j, V_j = 2j+1).
+          // A group of fills shares the full and the empty barrier of its last fill's
+          // slot: the groups are {K_0}, {V_0, K_1}, ..., {V_{n-1}}, as the issuing
+          // thread consumes them
+          for (int i0 = 0; i0 < 2 * n_tiles && ok;) {
+            const uint32_t nf = ((i0 & 1) && i0 + 1 < 2 * n_tiles) ? 2u : 1u;
+            const int gs = (int)((kv_it + nf - 1) % C::kStages);
+            for (uint32_t q = 0; q < nf && ok; ++q) {
+              const int x = (int)((kv_it + q) % C::kStages);
+              if ((filled >> x) & 1u)
+                ok = sy.wait(B_KV + C::kStages + (((rel_next >> x) & 1u) ? (x + 1) % C::kStages : x),
+                             (rel_par >> x) & 1u);
+            }
+            if (!ok) break;
+            const uint32_t ep = (e_cnt >> gs) & 1u;   // parity of the empty phase that releases this group
+            e_cnt ^= 1u << gs;
+            const uint32_t fbar = sy.bar(B_KV + gs);
+            ptx::mbar_arrive_expect_tx(fbar, nf * (uint32_t)C::kTileBytes);
+            f_cnt ^= 1u << gs;
+            f_used |= 1u << gs;
+            for (uint32_t q = 0; q < nf; ++q) {
+              const int x = (int)((kv_it + q) % C::kStages);
+              const int i = i0 + (int)q;
+              filled |= 1u << x;
+              rel_next = (rel_next & ~(1u << x)) | ((x != gs ? 1u : 0u) << x);
+              rel_par = (rel_par & ~(1u << x)) | (ep << x);
+              const bool is_v = i & 1;
+              const void* map = is_v ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k);
+              const int row = (is_v ? u.off_v : u.off_k) + (u.kv_lo + (i >> 1)) * BN;
+  #pragma unroll
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                ptx::tma_load_3d(sbase + C::kOffKV + x * C::kTileBytes + hf * BN * 128, map, fbar, hf * 64, u.g, row);
+            }
+            kv_it += nf;
+            i0 += (int)nf;
           }
         }
+        THD_UNIT_STAMP(it, 1);
         if (!ok) break;
       }
       // loads complete whether or not anyone consumes them; on an abort wait for
       // the ones still in flight before the CTA may exit
       if (*abort_flag) {
         for (int s = 0; s < C::kStages; ++s) {
-          if (kv_it > (uint32_t)s) {
-            const uint32_t last = (kv_it - 1 - (uint32_t)s) / C::kStages * C::kStages + (uint32_t)s;
+          // the last phase armed on full barrier s
+          bool armed;
+          uint32_t parity;
+          if constexpr (C::kGroupKV) {
+            armed = (f_used >> s) & 1u;
+            parity = ((f_cnt >> s) & 1u) ^ 1u;
+          } else {
+            armed = kv_it > (uint32_t)s;
+            const uint32_t last = armed ? (kv_it - 1 - (uint32_t)s) / C::kStages * C::kStages + (uint32_t)s : 0u;
+            parity = (last / C::kStages) & 1u;
+          }
+          if (armed) {
             const uint64_t t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(sy.bar(B_KV + s), (last / C::kStages) & 1u) &&
-                   ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+            while (!ptx::mbar_try_wait(sy.bar(B_KV + s), parity) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
             }
           }
         }
@@ -359,8 +435,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             ptx::mma_ts(dO, aP + kk * 8, va + (uint64_t)(kk * 128), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
+      // ring slot and phase of a fill (one barrier pair per slot); with kGroupKV a
+      // group of fills ({K_0}, {V_j, K_{j+1}}, {V_{n-1}}) is signalled and released by
+      // the barriers of its last fill's slot, whose full phases are counted per slot
+      // (parity bit in f_par)
       auto kv_stage = [](uint32_t fill) { return (int)(fill % C::kStages); };
       auto kv_phase = [](uint32_t fill) { return (fill / C::kStages) & 1u; };
+      uint32_t f_par = 0;
+      auto wait_group = [&](int gs) -> bool {
+        const bool r = sy.wait(B_KV + gs, (f_par >> gs) & 1u);
+        f_par ^= 1u << gs;
+        return r;
+      };
       uint32_t q_uses[2] = {0, 0}, p_waits[2] = {0, 0}, o_reads_seen[2] = {0, 0}, o_read_waits[2] = {0, 0};
       uint32_t kv_base = 0;
       bool issued_any = false, ok = true;
@@ -381,6 +467,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const UnitInfo u = info[slot];
         ptx::mbar_arrive(sy.bar(B_SCHED_EMPTY + slot));
         if (u.w >= num_tiles) break;
+        THD_UNIT_STAMP(it, 2);
         // sub-tile t visits loop indices [tl[t], te[t]); with a left window the
         // second sub-tile may start later than the first
         const int nt[2] = {u.n_kv[0], u.n_kv[1]};
@@ -388,13 +475,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int te[2] = {tl[0] + nt[0], tl[1] + nt[1]};
         const int n_tiles = u.n_tiles;
         if (n_tiles == 0) continue;
-        ok = sy.wait(B_KV + kv_stage(kv_base), kv_phase(kv_base));
+        if constexpr (C::kGroupKV) ok = wait_group(kv_stage(kv_base));
+        else ok = sy.wait(B_KV + kv_stage(kv_base), kv_phase(kv_base));
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (ok && nt[t] > 0 && (!WIN || tl[t] == 0)) ok = first_qk(t, kv_stage(kv_base), nt[t]);
         if (!ok) break;
         ptx::tc_commit(sy.bar(B_KV + C::kStages + kv_stage(kv_base)));
         issued_any = true;
+        THD_UNIT_STAMP(it, 3);
         for (int j = 0; j < n_tiles && ok; ++j) {
           THD_TRACE_STAMP(2, j, 0, it);
           const uint32_t vfill = kv_base + 2u * (uint32_t)j + 1u;
@@ -402,7 +491,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           const int vstage = kv_stage(vfill);
           const int kstage = kv_stage(kfill);
           const bool kmore = j + 1 < n_tiles;
-          ok = sy.wait(B_KV + vstage, kv_phase(vfill)) && (!kmore || sy.wait(B_KV + kstage, kv_phase(kfill)));
+          const int gstage = kmore ? kstage : vstage;
+          if constexpr (C::kGroupKV) ok = wait_group(gstage);
+          else ok = sy.wait(B_KV + vstage, kv_phase(vfill)) && (!kmore || sy.wait(B_KV + kstage, kv_phase(kfill)));
           if (!ok) break;
           THD_TRACE_STAMP(2, j, 1, it);
           // keys of this tile that exist: PV runs over ceil(valid/16) steps of 16
@@ -449,10 +540,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               if (ok && kmore && nt[t] > 0 && tl[t] == j + 1) ok = first_qk(t, kstage, nt[t]);
           }
           if (!ok) break;
-          ptx::tc_commit(sy.bar(B_KV + C::kStages + vstage));
-          if (kmore) ptx::tc_commit(sy.bar(B_KV + C::kStages + kstage));
+          if constexpr (C::kGroupKV) {
+            ptx::tc_commit(sy.bar(B_KV + C::kStages + gstage));
+          } else {
+            ptx::tc_commit(sy.bar(B_KV + C::kStages + vstage));
+            if (kmore) ptx::tc_commit(sy.bar(B_KV + C::kStages + kstage));
+          }
           THD_TRACE_STAMP(2, j, 6, it);
         }
+        THD_UNIT_STAMP(it, 4);
         kv_base += 2u * (uint32_t)n_tiles;
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -685,12 +781,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994530942f : -INFINITY;
         p.stats[(int64_t)(e_off_s + er) * p.stats_tok + (int64_t)e_h * p.stats_head] = lse;
       }
+#ifdef THD_FWD_TRACE
+      if ((warp & 3) == 0 && lane == 0) THD_UNIT_STAMP(it, 5 + t);
+#endif
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  if (threadIdx.x == 0) THD_CTA_STAMP(1);
   if (warp == kAllocWarp) {
     __syncwarp();
     ptx::tmem_dealloc(tmem, 512);
@@ -726,8 +826,18 @@ extern "C" int thd_fwd_trace_read(void* host, size_t bytes) {
 }
 extern "C" int thd_fwd_trace_clear() {
   void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_fwd_trace) != cudaSuccess) return 1;
-  return (int)cudaMemset(p, 0, sizeof(g_fwd_trace));
+  if (cudaGetSymbolAddress(&p, g_fwd_trace) != cudaSuccess || cudaMemset(p, 0, sizeof(g_fwd_trace)) != cudaSuccess)
+    return 1;
+  if (cudaGetSymbolAddress(&p, g_fwd_units) != cudaSuccess || cudaMemset(p, 0, sizeof(g_fwd_units)) != cudaSuccess)
+    return 1;
+  if (cudaGetSymbolAddress(&p, g_fwd_cta) != cudaSuccess) return 1;
+  return (int)cudaMemset(p, 0, sizeof(g_fwd_cta));
+}
+// unit timeline (g_fwd_units) followed by the CTA spans (g_fwd_cta)
+extern "C" int thd_fwd_trace_units_read(void* host, size_t bytes) {
+  if (bytes < sizeof(g_fwd_units) + sizeof(g_fwd_cta)) return 1;
+  if (cudaMemcpyFromSymbol(host, g_fwd_units, sizeof(g_fwd_units)) != cudaSuccess) return 1;
+  return (int)cudaMemcpyFromSymbol(static_cast<char*>(host) + sizeof(g_fwd_units), g_fwd_cta, sizeof(g_fwd_cta));
 }
 #endif
 int tc_grid_size(int num_sms, int max_pairs, int h_q) {

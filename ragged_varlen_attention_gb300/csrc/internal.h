@@ -18,7 +18,7 @@ namespace thd {
 // being the pair count.
 enum HeaderWord : int {
   kHdrCounter = 0, kHdrStatus = 1, kHdrNumPairs = 2, kHdrNumTiles = 3, kHdrGroupStart = 4,
-  kHdrNumSplit = 16  // pairs whose KV range is split in two (partials merged by the combine kernel)
+  kHdrNumSplit = 16  // pairs whose KV range is split (partials merged by the combine kernel)
 };
 constexpr int kCostGroups = 11;
 constexpr int kHeaderBytes = 128;
@@ -27,11 +27,22 @@ static_assert((kHdrNumSplit + 1) * 4 <= kHeaderBytes, "header words");
 
 // KV split: when a launch has fewer than kSplitWaves waves of units, every pair
 // visiting at least kMinSplitCost KV tiles is processed as two halves of its KV
-// range whose partial results are merged afterwards. kMaxSmsForSizing bounds the
-// SM count the workspace is sized for.
+// range whose partial results are merged afterwards. When the halves then leave a
+// last, partial wave of units (and at least one full wave before it), the
+// cheapest split pairs whose units would fill that wave are cut into kTailParts
+// parts instead, so the end of the launch is filled with short units rather than
+// leaving CTAs idle; only pairs of at least kMinTailCost tiles qualify.
+// kMaxSmsForSizing bounds the SM count the workspace is sized for.
 constexpr int kSplitWaves = 4;
 constexpr int kMinSplitCost = 16;   // each half keeps >= 8 tiles to amortise a unit's fill and epilogue
+constexpr int kTailParts = 8;
+constexpr int kMinTailCost = 8 * kTailParts;
 constexpr int kMaxSmsForSizing = 160;
+// split pairs cut into kTailParts parts at most: the last wave holds fewer than
+// kMaxSmsForSizing units, i.e. fewer than that many half entries of h_q units each
+__host__ __device__ constexpr int max_tail_pairs(int unit_heads) {
+  return ((kMaxSmsForSizing + unit_heads - 1) / unit_heads + 1) / 2;
+}
 
 // Per-sequence record written by the setup kernel. `shift` is the causal shift:
 // query row i sees keys j < len_k with j <= i + shift (mask 0 stores len_k, which
@@ -48,17 +59,19 @@ static_assert(sizeof(SeqMeta) == 48, "SeqMeta is 48 bytes");
 constexpr int32_t kNoLowerBound = -(1 << 30);
 
 // A scheduled unit: rows [row0, row0 + rows_per_unit) of sequence b, for every
-// query head. `split` = (half << 8) | halves: halves is 1 for a whole pair, 2 when
-// the pair's KV range [0, n) is processed as [0, n/2) and [n/2, n); `part` is
-// the pair's slot in the partial-result buffers (-1 when whole).
+// query head. `split` = (i << 8) | parts: parts is 1 for a whole pair, else the
+// pair's KV tile span [0, n) is processed in `parts` pieces and this entry covers
+// [i n / parts, (i + 1) n / parts); `part` is the entry's slot in the
+// partial-result buffers (-1 when whole).
 struct PairRec {
   int32_t b, row0, split, part;
 };
 static_assert(sizeof(PairRec) == 16, "PairRec is 16 bytes");
 
-// A pair whose KV range was split: where its rows are, for the combine kernel.
+// A pair whose KV range was split, for the combine kernel: where its rows are and
+// its partial slots [slot0, slot0 + parts).
 struct SplitRec {
-  int32_t b, row0;
+  int32_t b, row0, slot0, parts;
 };
 
 constexpr int kCostBins = 1024;          // LPT buckets of the setup kernel's counting sort
@@ -90,6 +103,9 @@ struct SetupParams {
   int64_t tok_stride[5];    // Q K V O Stats token strides (elements), for element offsets
   int32_t num_ctas;         // persistent CTAs of the attention kernel
   int32_t max_split;        // capacity of the split-pair table
+  int32_t max_tail;         // split pairs that may be cut into kTailParts parts
+  int32_t pair_cap;         // capacity of the pair list (scheduled entries)
+  int32_t slot_cap;         // partial-result slots (split parts)
   // key axis of the backward: consecutive sequences with the same K and V offsets
   // read the same key rows (zigzag context-parallel chunks of one document) and
   // form one group whose dK/dV units sum over all of its members; K/V rows of
@@ -98,7 +114,7 @@ struct SetupParams {
   uint32_t* header;
   SeqMeta* meta;
   int32_t* pair_base;       // [batch + 1]
-  PairRec* pairs;           // [2 * max_pairs when splitting is allowed, else max_pairs]
+  PairRec* pairs;           // [pair_cap]
   SplitRec* splits;         // [max_split]
 };
 
@@ -120,8 +136,8 @@ struct FwdParams {
   const SeqMeta* meta;
   const PairRec* pairs;
   const SplitRec* splits;
-  float* part_o;            // [max_split][2][h_q][rows_per_unit][d] normalised partial O
-  float* part_lse;          // [max_split][2][h_q][rows_per_unit] partial LSE, base 2
+  float* part_o;            // [slots][h_q][rows_per_unit][d] normalised partial O
+  float* part_lse;          // [slots][h_q][rows_per_unit] partial LSE, base 2
   int32_t rows_per_unit;
   int32_t test_stall;       // test hook: see THD_FLAG_TEST_STALL
   int32_t has_window;       // a window tensor was passed (some lo_shift may be bounded)
@@ -220,6 +236,7 @@ __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return
 
 // Launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_setup(const SetupParams& p, cudaStream_t stream);
+
 cudaError_t launch_fwd_simt(const FwdParams& p, thd_dtype_t dtype, int rows_per_unit, int num_sms,
                             cudaStream_t stream);
 int simt_rows_per_unit(int d);
@@ -246,6 +263,9 @@ struct thd_attn_plan_s {
   int64_t ws_off[7];        // header, meta, pair_base, pairs, splits, part_o, part_lse
   int32_t allow_split;
   int32_t max_split;
+  int32_t max_tail;
+  int32_t pair_cap;         // pair list entries: max_pairs, or with splits every part of every pair
+  int32_t slot_cap;         // partial-result slots
   // backward plans (thd_attn_plan_bwd)
   int32_t is_bwd;
   int64_t g_cap_rows[4];    // dO, dQ, dK, dV

@@ -122,6 +122,11 @@ __device__ __forceinline__ bool same_keys(const SetupParams& p, int32_t e) {
   return e > 0 && p.off_k[e] == p.off_k[e - 1] && p.off_v[e] == p.off_v[e - 1];
 }
 
+// tiles of part i of a pair of `cost` tiles cut into n parts ([i c / n, (i + 1) c / n))
+__device__ __forceinline__ int32_t part_cost(int32_t cost, int32_t i, int32_t n) {
+  return (int32_t)(((int64_t)(i + 1) * cost) / n - ((int64_t)i * cost) / n);
+}
+
 // group of a (clamped) cost: 0 for 512..1023, 1 for 256..511, ..., 9 for 1, 10 for 0
 __device__ __forceinline__ int cost_group(int32_t c) { return c == 0 ? kCostGroups - 1 : 9 - (31 - __clz(c)); }
 
@@ -138,8 +143,9 @@ __device__ __forceinline__ int32_t find_seq(const int32_t* pair_base, int32_t ba
 __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   __shared__ uint32_t hist[kCostBins];
   __shared__ uint32_t group_count[kCostGroups];
-  __shared__ uint32_t n_splittable, n_split_done;
-  __shared__ bool split_on;
+  __shared__ uint32_t n_splittable, n_split_done, n_slots, n_slots_need;
+  __shared__ bool split_on, sched_ok;
+  __shared__ int32_t tail_need, tail_cost, tail_ties, tail_tie_count, tail_e, tie_seen;
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   __shared__ uint32_t status_s;
@@ -327,24 +333,101 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
                (int64_t)total * p.unit_heads < (int64_t)kSplitWaves * p.num_ctas && n_splittable > 0 &&
                (int32_t)n_splittable <= p.max_split;
     n_split_done = 0;
+    n_slots = 0;
+    n_slots_need = 0;
+    tail_cost = -1;
+    tail_ties = tail_tie_count = 0;
+    tail_e = 0;
+    tie_seen = 0;
+    // units of a last, partial wave after halving: the `need` cheapest split pairs
+    // (costs ascending, then the highest pair index first) are cut into kTailParts
+    tail_need = 0;
+    if (split_on) {
+      const int64_t units = ((int64_t)total + n_splittable) * p.unit_heads;
+      const int64_t rest = units % p.num_ctas;
+      if (units >= p.num_ctas && rest > 0) {
+        const int64_t entries = (rest + p.unit_heads - 1) / p.unit_heads;
+        tail_need = (int32_t)min64((entries + 1) / 2, (int64_t)p.max_tail);
+      }
+    }
   }
   __syncthreads();
 
-  // 2b. cost histogram over the scheduled entries (a split pair gives two)
+  // 2a'. tail pairs: cost histogram of the split pairs (one bucket per thread), an
+  // inclusive scan finds the cost c_t at which `need` pairs are reached; among pairs
+  // of cost c_t the ones with the highest index are taken (threshold index tail_e)
+  if (tail_need > 0) {
+    for (int32_t e = tid; e < total; e += blockDim.x) {
+      const int32_t b = find_seq(p.pair_base, p.batch, e);
+      const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
+      const int32_t c = pair_cost(p, b, row0);
+      if (c >= kMinSplitCost) atomicAdd(&hist[min(c, kCostBins - 1)], 1u);
+    }
+    __syncthreads();
+    const int32_t cnt = (int32_t)hist[tid];
+    const int32_t incl = block_inclusive_scan(cnt, warp_sums);
+    if (incl >= tail_need && incl - cnt < tail_need) {
+      // the cheapest tail pairs must be long enough for kTailParts parts; the
+      // clamped top bucket cannot order its pairs, so it takes no tail split
+      if (tid >= kMinTailCost && tid < kCostBins - 1) {
+        tail_cost = tid;
+        tail_ties = tail_need - (incl - cnt);   // pairs of cost c_t to take
+        tail_tie_count = cnt;
+      }
+    }
+    __syncthreads();
+    hist[tid] = 0;
+    if (tail_cost >= 0 && tail_ties < tail_tie_count) {
+      // rank the pairs of cost c_t by index, from the end: the tail_ties highest are taken
+      for (int32_t base = 0; base < total; base += blockDim.x) {
+        const int32_t e = base + tid;
+        int32_t tie = 0;
+        if (e < total) {
+          const int32_t b = find_seq(p.pair_base, p.batch, e);
+          const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
+          tie = pair_cost(p, b, row0) == tail_cost ? 1 : 0;
+        }
+        const int32_t incl_t = block_inclusive_scan(tie, warp_sums);
+        const int32_t rank = tie_seen + incl_t - 1;      // among the ties, from the front
+        if (tie && tail_tie_count - 1 - rank == tail_ties - 1) tail_e = e;
+        __syncthreads();
+        if (tid == blockDim.x - 1) tie_seen += incl_t;
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+  }
+  // parts of a pair of cost c at index e (pairs below kMinTailCost keep two)
+  auto parts_of = [&](int32_t c, int32_t e) -> int32_t {
+    if (!split_on || c < kMinSplitCost) return 1;
+    if (tail_cost >= 0 && c >= kMinTailCost && (c < tail_cost || (c == tail_cost && e >= tail_e)))
+      return kTailParts;
+    return 2;
+  };
+
+  // 2b. cost histogram over the scheduled entries (a pair in n parts gives n)
   for (int32_t e = tid; e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
     const int32_t cost = pair_cost(p, b, row0);
-    if (split_on && cost >= kMinSplitCost) {
-      const int32_t c0 = min(cost / 2, kCostBins - 1), c1 = min(cost - cost / 2, kCostBins - 1);
-      atomicAdd(&hist[c0], 1u);
-      atomicAdd(&hist[c1], 1u);
-      atomicAdd(&group_count[cost_group(c0)], 1u);
-      atomicAdd(&group_count[cost_group(c1)], 1u);
-    } else {
-      const int32_t c = min(cost, kCostBins - 1);
+    const int32_t n = parts_of(cost, e);
+    if (n > 1) atomicAdd(&n_slots_need, (uint32_t)n);
+    for (int32_t i = 0; i < n; ++i) {
+      const int32_t c = min(part_cost(cost, i, n), kCostBins - 1);
       atomicAdd(&hist[c], 1u);
       atomicAdd(&group_count[cost_group(c)], 1u);
+    }
+  }
+  __syncthreads();
+  // the pair list and the partial slots are sized at plan time for every entry; a
+  // schedule that does not fit is a TILE_OVERFLOW and gets no work at all
+  if (tid == 0) {
+    uint32_t entries = 0;
+    for (int g = 0; g < kCostGroups; ++g) entries += group_count[g];
+    sched_ok = entries <= (uint32_t)p.pair_cap && n_slots_need <= (uint32_t)max(p.slot_cap, 0);
+    if (!sched_ok) {
+      atomicOr(&status_s, (uint32_t)THD_DEV_TILE_OVERFLOW);
+      for (int g = 0; g < kCostGroups; ++g) group_count[g] = 0;
     }
   }
   __syncthreads();
@@ -359,20 +442,22 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
   __syncthreads();
 
   // 4. scatter
-  for (int32_t e = tid; e < total; e += blockDim.x) {
+  for (int32_t e = tid; sched_ok && e < total; e += blockDim.x) {
     const int32_t b = find_seq(p.pair_base, p.batch, e);
     const int32_t row0 = (e - p.pair_base[b]) * p.rows_per_unit;
     const int32_t cost = pair_cost(p, b, row0);
-    if (split_on && cost >= kMinSplitCost) {
+    const int32_t n = parts_of(cost, e);
+    if (n > 1) {
       const int32_t part = (int32_t)atomicAdd(&n_split_done, 1u);
+      const int32_t slot0 = (int32_t)atomicAdd(&n_slots, (uint32_t)n);
       SplitRec sr;
-      sr.b = b; sr.row0 = row0;
+      sr.b = b; sr.row0 = row0; sr.slot0 = slot0; sr.parts = n;
       p.splits[part] = sr;
-      for (int half = 0; half < 2; ++half) {
-        const int32_t c = min(half == 0 ? cost / 2 : cost - cost / 2, kCostBins - 1);
+      for (int32_t i = 0; i < n; ++i) {
+        const int32_t c = min(part_cost(cost, i, n), kCostBins - 1);
         const uint32_t slot = atomicAdd(&hist[c], 1u);
         PairRec r;
-        r.b = b; r.row0 = row0; r.split = (half << 8) | 2; r.part = part;
+        r.b = b; r.row0 = row0; r.split = (i << 8) | n; r.part = slot0 + i;
         p.pairs[slot] = r;
       }
     } else {
@@ -395,7 +480,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(SetupParams p) {
     p.header[kHdrStatus] = status_s;
     p.header[kHdrNumPairs] = acc;
     p.header[kHdrNumTiles] = acc * (uint32_t)p.unit_heads;
-    p.header[kHdrNumSplit] = split_on ? n_splittable : 0u;
+    p.header[kHdrNumSplit] = split_on && sched_ok ? n_splittable : 0u;
   }
 }
 

@@ -5,6 +5,9 @@ the library with the kernel's clock64() stamps compiled in (-DTHD_FWD_TRACE, und
 _build/trace), runs the workload's forward pass (default cp_chunks) and prints, as
 medians over CTAs and KV tiles 4..59 of each CTA's first unit, how long the softmax
 warps and the MMA-issuing thread spend in each phase of a tile, in SM clock cycles.
+With ``--units`` it prints instead where the launch's time goes unit by unit
+(%globaltimer, ns): CTA start and end against the earliest start, and per unit the
+wait from claim to first MMA, the tile loop, and the epilogue.
 The library itself is built without the stamps.
 """
 from __future__ import annotations
@@ -21,6 +24,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 PKG = os.path.dirname(HERE)
 ROOT = os.path.dirname(PKG)
 CTAS, ROLES, TILES, EVENTS = 160, 3, 64, 8
+UNITS, UEVENTS = 16, 8
 
 
 def build_traced() -> str:
@@ -42,7 +46,9 @@ def build_traced() -> str:
 
 def main() -> int:
     import torch
-    name = sys.argv[1] if len(sys.argv) > 1 else "cp_chunks"
+    args = [a for a in sys.argv[1:] if not a.startswith("--")]
+    units_mode = "--units" in sys.argv[1:]
+    name = args[0] if args else "cp_chunks"
     lib_path = build_traced()
     from ragged_varlen_attention_gb300 import binding as bd
     from ragged_varlen_attention_gb300 import workloads as wl
@@ -66,6 +72,9 @@ def main() -> int:
         bd.thd_attn_fwd(plan, q, k, v, o, st, *meta, mask, qco, ws)
     status = bd.thd_attn_read_status(plan, ws)
     torch.cuda.synchronize()
+    if units_mode:
+        return report_units(lib, name, status, int(os.environ.get("THD_TRACE_SMS", "0")) or
+                            torch.cuda.get_device_properties(0).multi_processor_count)
     buf = np.zeros(CTAS * ROLES * TILES * EVENTS, dtype=np.uint64)
     if lib.thd_fwd_trace_read(buf.ctypes.data, buf.nbytes) != 0:
         raise RuntimeError("trace read failed")
@@ -92,6 +101,51 @@ def main() -> int:
     print(f"P0 stored -> issuer past its wait {med(i[:, span, 2] - s0[:, span, 5]):6.0f}; "
           f"P1 {med(i[:, span, 4] - s1[:, span, 5]):6.0f}; batch 0 issued -> S0(j+1) seen "
           f"{med(s0[:, 5:61, 1] - i[:, 4:60, 3]):5.0f}; batch 1 -> S1(j+1) {med(s1[:, 5:61, 1] - i[:, 4:60, 5]):5.0f}")
+    return 0
+
+
+def report_units(lib, name: str, status: int, n_sms: int) -> int:
+    lib.thd_fwd_trace_units_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    buf = np.zeros(CTAS * UNITS * UEVENTS + CTAS * 2, dtype=np.uint64)
+    if lib.thd_fwd_trace_units_read(buf.ctypes.data, buf.nbytes) != 0:
+        raise RuntimeError("trace read failed")
+    u = buf[:CTAS * UNITS * UEVENTS].reshape(CTAS, UNITS, UEVENTS)
+    cta = buf[CTAS * UNITS * UEVENTS:].reshape(CTAS, 2)[:n_sms].astype(np.int64)
+    n_sms = int((cta[:, 0] > 0).sum())           # CTAs of the launch (grid <= SMs)
+    cta = cta[:n_sms]
+    t0 = int(cta[:, 0].min())
+    rel = lambda x: (x.astype(np.int64) - t0) / 1000.0    # microseconds after the earliest CTA start
+    start, end = rel(cta[:, 0]), rel(cta[:, 1])
+    print(f"workload {name}, status {status}; times in us after the earliest CTA start")
+    print(f"CTA start: min {start.min():.2f} median {np.median(start):.2f} max {start.max():.2f}; "
+          f"CTA end: min {end.min():.2f} median {np.median(end):.2f} max {end.max():.2f}")
+    rows = []
+    for c in range(n_sms):
+        for k in range(UNITS):
+            ev = u[c, k]
+            if ev[2] == 0 or ev[3] == 0:      # not reached, or a unit without KV tiles
+                continue
+            tiles = int(ev[7] & 0xffffffff)
+            epi = max(int(ev[5]), int(ev[6]))
+            rows.append((c, k, tiles, rel(ev[0]), rel(ev[2]), rel(ev[3]), rel(ev[4]), rel(np.uint64(epi)) if epi else np.nan))
+    a = np.array([r[2:] for r in rows], dtype=np.float64)
+    n_units = np.bincount([r[0] for r in rows], minlength=n_sms)
+    print(f"units per CTA: min {n_units.min()} median {np.median(n_units):.0f} max {n_units.max()}")
+    tiles, claim, got, first, last, epi = a.T
+    print(f"per unit (medians): claim -> first QK committed {np.median(first - claim):.2f}; "
+          f"first QK -> last MMA committed {np.median(last - first):.2f} for {np.median(tiles):.0f} tiles; "
+          f"last MMA -> epilogue stored {np.nanmedian(epi - last):.2f}")
+    for n in sorted(set(tiles.astype(int))):
+        m = tiles == n
+        print(f"  {n:3d} tiles: {int(m.sum()):4d} units, loop {np.median(last[m] - first[m]):6.2f} us "
+              f"({np.median(last[m] - first[m]) / max(n, 1):.2f} per tile), claim -> first QK "
+              f"{np.median(first[m] - claim[m]):5.2f}, epilogue {np.nanmedian(epi[m] - last[m]):5.2f}")
+    worst = int(np.argmax(end))
+    print(f"last CTA to finish ({worst}, end {end[worst]:.2f}):")
+    for r in rows:
+        if r[0] == worst:
+            print(f"  unit {r[1]}: {r[2]} tiles, claimed {r[3]:.2f}, first QK {r[5]:.2f}, last MMA {r[6]:.2f}, "
+                  f"stored {r[7]:.2f}")
     return 0
 
 

@@ -52,22 +52,42 @@ BAD_LENGTH, BAD_OFFSET, BAD_MASK, TILE_OVERFLOW = 1, 2, 4, 8
 
 
 SPLIT_WAVES, MIN_SPLIT_COST = 4, 16
+TAIL_PARTS, MIN_TAIL_COST, MAX_SMS_FOR_SIZING = 8, 64, 160
+
+
+def part_cost(cost: int, i: int, n: int) -> int:
+    """Tiles of part i of a pair of `cost` tiles cut into n parts."""
+    return (i + 1) * cost // n - i * cost // n
 
 
 def split_entries(pairs, h_q: int, num_ctas: int, max_split: int, allow_split: bool):
-    """Scheduled entries after the KV-split decision: list of (b, row0, half, halves,
+    """Scheduled entries after the KV-split decision: list of (b, row0, part, parts,
     cost) and the number of split pairs. Pairs visiting at least MIN_SPLIT_COST KV
-    tiles are halved when the launch has fewer than SPLIT_WAVES waves of units."""
+    tiles are halved when the launch has fewer than SPLIT_WAVES waves of units. When
+    the halves leave a partial last wave after at least one full one, the cheapest
+    split pairs that fill it (ascending cost, then descending index in the pair list)
+    are cut into TAIL_PARTS parts, provided the threshold cost is at least
+    MIN_TAIL_COST and below the clamped top bucket; pairs below MIN_TAIL_COST keep two."""
     splittable = [p for p in pairs if p[2] >= MIN_SPLIT_COST]
     on = (allow_split and len(pairs) > 0 and len(pairs) * h_q < SPLIT_WAVES * num_ctas
           and 0 < len(splittable) <= max_split)
+    tail = set()
+    if on:
+        units = (len(pairs) + len(splittable)) * h_q
+        rest = units % num_ctas
+        if units >= num_ctas and rest > 0:
+            max_tail = min(max_split, (-(-MAX_SMS_FOR_SIZING // h_q) + 1) // 2)
+            need = min((-(-rest // h_q) + 1) // 2, max_tail)
+            cand = sorted((c, -e) for e, (_, _, c) in enumerate(pairs) if c >= MIN_SPLIT_COST)
+            if 0 < need <= len(cand) and MIN_TAIL_COST <= cand[need - 1][0] < COST_BINS - 1:
+                tail = {-ne for c, ne in cand[:need] if c >= MIN_TAIL_COST}
     out = []
-    for b, r, c in pairs:
-        if on and c >= MIN_SPLIT_COST:
-            out.append((b, r, 0, 2, min(c // 2, COST_BINS - 1)))
-            out.append((b, r, 1, 2, min(c - c // 2, COST_BINS - 1)))
-        else:
+    for e, (b, r, c) in enumerate(pairs):
+        n = 1 if not (on and c >= MIN_SPLIT_COST) else (TAIL_PARTS if e in tail else 2)
+        if n == 1:
             out.append((b, r, 0, 1, c))
+        else:
+            out.extend((b, r, i, n, min(part_cost(c, i, n), COST_BINS - 1)) for i in range(n))
     return out, (len(splittable) if on else 0)
 
 

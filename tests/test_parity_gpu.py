@@ -9,6 +9,7 @@ from ragged_varlen_attention_gb300 import binding as bd
 from ragged_varlen_attention_gb300 import workloads as wl
 from tests import schedule_mirror
 from tests.gpu_harness import TOL, check_parity, check_untouched, run_thd
+from tests.helpers import max_abs_finite
 
 pytestmark = pytest.mark.gpu
 
@@ -130,6 +131,27 @@ def test_split_ragged_packs(seed):
     check_untouched(batch, res)
 
 
+def test_tail_split_parts():
+    """Long-context chunks whose halved key ranges leave a partial last wave: the
+    cheapest pairs are processed in eight parts (checked in the tile list) and merged
+    by the combine kernel; sampled rows against the oracle, every row against the
+    unsplit path, and no other byte of O and Stats touched."""
+    batch = wl.make("cp_chunks", **TAIL_CASE)
+    res = run_thd(batch)
+    assert res["status"] == 0
+    hdr, _, _, pairs_off = res["plan"].workspace_layout
+    ws = res["ws"].cpu().numpy()
+    n_entries = int(ws[hdr:hdr + 128].view(np.uint32)[2])
+    parts = ws[pairs_off:pairs_off + 16 * n_entries].view(np.int32).reshape(n_entries, 4)[:, 2] & 0xFF
+    assert (parts == 8).sum() > 0 and (parts == 2).sum() > 0
+    check_parity(batch, res, row_subset=_sample_rows(batch, seed=7))
+    check_untouched(batch, res)
+    ref = run_thd(batch, flags=bd.FLAG_NO_KV_SPLIT)
+    assert ref["status"] == 0
+    assert max_abs_finite(res["o"].float().numpy(), ref["o"].float().numpy()) <= 2e-2
+    assert max_abs_finite(res["stats"].numpy(), ref["stats"].numpy()) <= 1e-3
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_kv_interleaved_view_equals_contiguous(kernel):
     """K/V as views of an interleaved [T, 2, H, D] buffer (token stride 2*H*D) give
@@ -141,11 +163,15 @@ def test_kv_interleaved_view_equals_contiguous(kernel):
     assert torch.equal(a["stats"].view(torch.int32), b["stats"].view(torch.int32))
 
 
+TAIL_CASE = dict(docs=2, k_len=16384, q_len=1536, h=16)
+
 SCHEDULE_CASES = [
     ("mixed_gqa", {}, bd.KERNEL_AUTO, 0),                      # many units: no split
     ("mixed_gqa", {}, bd.KERNEL_SIMT, 0),
     ("cp_chunks", dict(docs=2, k_len=2048, q_len=768, h=4), bd.KERNEL_AUTO, 0),   # split
     ("cp_chunks", dict(docs=2, k_len=2048, q_len=768, h=4), bd.KERNEL_AUTO, bd.FLAG_NO_KV_SPLIT),
+    # 12 pairs of ~128 tiles, 16 heads: halves give 2.5 waves, the last wave's pairs in 8 parts
+    ("cp_chunks", TAIL_CASE, bd.KERNEL_AUTO, 0),
 ]
 
 
@@ -171,21 +197,24 @@ def test_schedule_matches_cpu_mirror(name, kw, kernel, flags):
     meta = ws[meta_off:meta_off + 48 * batch.batch].view(np.int32).reshape(batch.batch, 12)
     assert np.array_equal(meta, meta_exp)
     recs = ws[pairs_off:pairs_off + 16 * n_exp].view(np.int32).reshape(n_exp, 4)
-    # same multiset of (b, row0, half, halves); costs non-increasing along the list;
-    # the two halves of a split pair share one partial slot, slots are 0..n_split-1
-    cost = {(b, r, hf, hs): c for b, r, hf, hs, c in entries}
+    # same multiset of (b, row0, part, parts); costs non-increasing along the list;
+    # part i of a split pair has partial slot slot0 + i, and the slots of all split
+    # pairs are 0 .. (their parts) - 1
+    cost = {(b, r, i, n): c for b, r, i, n, c in entries}
     got = [(int(x[0]), int(x[1]), int(x[2]) >> 8, int(x[2]) & 0xFF) for x in recs]
     assert sorted(got) == sorted(cost)
     costs = [cost[g] for g in got]
     assert all(x >= y for x, y in zip(costs, costs[1:]))
-    parts = {}
+    slots = {}
     for g, x in zip(got, recs):
-        if g[3] == 2:
-            parts.setdefault((g[0], g[1]), set()).add(int(x[3]))
+        if g[3] > 1:
+            slots.setdefault((g[0], g[1]), {})[g[2]] = int(x[3])
         else:
             assert int(x[3]) == -1
-    assert all(len(v) == 1 for v in parts.values())
-    assert sorted(next(iter(v)) for v in parts.values()) == list(range(n_split))
+    assert len(slots) == n_split
+    for d in slots.values():
+        assert d == {i: d[0] + i for i in range(len(d))}
+    assert sorted(v for d in slots.values() for v in d.values()) == list(range(sum(len(d) for d in slots.values())))
 
 
 @pytest.mark.parametrize("name", ["cp_chunks", "mixed_gqa", "separate_padding"])
