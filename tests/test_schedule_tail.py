@@ -88,3 +88,26 @@ def test_tail_count_follows_last_wave_one_head():
     pairs = [(e, 0, 100) for e in range(300)]                 # 600 units: 3 waves + 144 -> 72 pairs
     entries, _ = sm.split_entries(pairs, 1, SMS, 640, True)
     assert sum(1 for n in _parts(entries).values() if n == 8) == 72
+
+
+def test_entries_and_slots_fit_the_plan_capacity():
+    """The pair list holds max_pairs + max_split + 6 max_tail entries and the partial
+    buffers 2 max_split + 6 max_tail slots (max_split = min(max_pairs, ceil(640 / h)),
+    max_tail = min(max_split, ceil((ceil(160 / h) + 1) / 2))): no pair list the rule can
+    see exceeds either, whatever the costs, heads and CTA count."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for _ in range(3000):
+        h = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 64]))
+        max_pairs = int(rng.integers(1, 400))
+        n = int(rng.integers(1, max_pairs + 1))
+        hi = int(rng.choice([20, 70, 200, 600, 1500]))
+        pairs = [(e, 0, int(c)) for e, c in enumerate(rng.integers(0, hi, size=n))]
+        num_ctas = min(int(rng.choice([148, 152, 160])), 2 * max_pairs * h)
+        max_split = min(max_pairs, -(-4 * 160 // h))
+        max_tail = min(max_split, (-(-160 // h) + 1) // 2)
+        entries, n_split = sm.split_entries(pairs, h, num_ctas, max_split, True)
+        assert len(entries) <= max_pairs + max_split + 6 * max_tail
+        slots = sum(1 for x in entries if x[3] > 1)
+        assert slots <= 2 * max_split + 6 * max_tail
+        assert sum(1 for x in entries if x[3] == 8) <= 8 * max_tail
