@@ -20,6 +20,9 @@
 // hold a full 128-column row of S without spilling.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D, 256+2D).
 // P (bf16/fp16, two per 32-bit column) overwrites the first 64 columns of its S.
+// Shared memory: Q0, Q1 and a ring of K/V tiles; at d = 128 each ring slot has its
+// own full/empty mbarrier pair, at d = 64 one pair covers the tiles V_j and K_{j+1}
+// that one tile's MMA batches consume (Cfg::kGroupKV).
 //
 // The issuing thread orders MMAs PV0(j), QK0(j+1), PV1(j), QK1(j+1): the two
 // sub-tiles alternate on the tensor core, and each softmax runs while the other

@@ -13,8 +13,11 @@
 //   4. scatter of every (sequence, first row) pair to its bucket's next slot.
 // When a launch has fewer than kSplitWaves waves of units and splitting is
 // allowed, long pairs are scheduled as two halves of their KV range (two entries,
-// one partial-result slot, one record for the combine kernel), which evens out
-// the last wave of the persistent grid.
+// a partial-result slot each, one record for the combine kernel), which evens out
+// the persistent grid; if the halves still leave a partial last wave, the cheapest
+// split pairs whose units would make it up are cut into kTailParts parts instead,
+// so short units fill the end of the launch. Entries and partial slots are checked
+// against the plan's capacities before anything is written.
 // It also zeroes the persistent scheduler's tile counter (header word 0) and
 // writes the status word, pair count and tile count. Invalid sequences get no
 // tiles and set a status bit; their rows are never touched.
