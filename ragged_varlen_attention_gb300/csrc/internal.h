@@ -38,8 +38,9 @@ constexpr int kMinSplitCost = 16;   // each half keeps >= 8 tiles to amortise a 
 constexpr int kTailParts = 8;
 constexpr int kMinTailCost = 8 * kTailParts;
 constexpr int kMaxSmsForSizing = 160;
-// split pairs cut into kTailParts parts at most: the last wave holds fewer than
-// kMaxSmsForSizing units, i.e. fewer than that many half entries of h_q units each
+// split pairs cut into kTailParts parts at most: the units of a last, partial wave
+// number rest < CTAs <= kMaxSmsForSizing, which are ceil(rest / unit_heads) half
+// entries of unit_heads units each, i.e. at most half as many pairs (rounded up)
 __host__ __device__ constexpr int max_tail_pairs(int unit_heads) {
   return ((kMaxSmsForSizing + unit_heads - 1) / unit_heads + 1) / 2;
 }
